@@ -1,0 +1,565 @@
+"""Benchmark of the paged GQA attention hot path on GB300.
+
+One step = one pass of the whole path over one batch: for every layer, kv_append_paged of the
+step's new tokens, attn_prefill_chunk of the prompt chunk, attn_decode_paged (split-KV + merge)
+of the decoding sequences. The default workload is the 28-layer mixed scheduler step
+(one 4,096-query chunk at offset 32,768 plus 31 decodes of 5,000..90,000 keys, each layer with
+its own K/V pools: about 173 GB of HBM), so every step reads far more than L2 holds.
+
+Reported (one JSON line from rank 0):
+  value      decode KV-read GB/s = sum of decode KV bytes / device time of the decode calls
+  prefill    chunked-prefill TFLOP/s = 4*D*Hq*(visible pairs) / device time of the prefill calls
+  roofline   the dominant kernel against the measured (else fallback) HBM / tensor peak
+  e2e        the same metrics through the public calls with pinned host buffers, per-step
+             host->device copies of the step's inputs and device->host copies of the results
+             inside the timed region
+  cpu_baseline  the fp64 oracle timed on a bounded sample on the host cores
+
+``--impl reference`` times the oracle itself (the only reference that exists for this path) on
+the same workload, one bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+# ----------------------------------------------------------------------------------------------
+# work accounting
+# ----------------------------------------------------------------------------------------------
+def decode_kv_bytes(seq_lens) -> int:
+    """Bytes the method must read: every cached key and value of every decoding sequence."""
+    return int(np.sum(seq_lens)) * W.kv_bytes_per_token()
+
+
+def prefill_pairs(seq_len: int, q_len: int) -> int:
+    """Visible (query, key) pairs of one chunk under bottom-right causal alignment."""
+    off = seq_len - q_len
+    return q_len * off + q_len * (q_len + 1) // 2
+
+
+def prefill_flops(pairs: int) -> float:
+    return 4.0 * W.HEAD_DIM * W.HQ * pairs  # QK^T and PV, 2 flops per MAC
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs")
+            bf = d.get("bf16_tflops")
+            bfs = d.get("bf16_tflops_sustained", bf)
+            if hbm and bf:
+                return float(hbm), float(bf), float(bfs), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "long_context_paged_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(kernel_file: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", kernel_file)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_hash") != src_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, out_path=None):
+        self.proc = None
+        self.path = out_path or os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, uuid=None):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if uuid and uuid not in parts[1]:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def device_uuid():
+    try:
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------------------------
+# the timed step
+# ----------------------------------------------------------------------------------------------
+class Step:
+    """Owns the workload on the device and runs/times one pass of the hot path."""
+
+    def __init__(self, pa, name, device):
+        self.pa = pa
+        self.name = name
+        self.inp = W.make_workload(name, device=device)
+        self.dev = device
+        inp = self.inp
+        L, ql = inp.host_seq_lens, inp.host_q_lens
+        self.is_chunk = ql > 1
+        self.chunk_idx = np.nonzero(self.is_chunk)[0]
+        self.dec_idx = np.nonzero(~self.is_chunk)[0]
+        assert len(self.chunk_idx) <= 1 and (len(self.chunk_idx) == 0 or self.chunk_idx[0] == 0), \
+            "the prompt chunk is the first sequence"
+        self.n_chunk_rows = int(ql[self.chunk_idx].sum()) if len(self.chunk_idx) else 0
+        self.layers = inp.layers
+        self.max_s = int(L.max())
+        self.append = name == "mixed_28l"
+        self.dec_bytes = decode_kv_bytes(L[self.dec_idx]) if len(self.dec_idx) else 0
+        self.pairs = sum(prefill_pairs(int(L[i]), int(ql[i])) for i in self.chunk_idx)
+        self.pf_flops = prefill_flops(self.pairs)
+        B = inp.batch
+        nd = len(self.dec_idx)
+        if nd:
+            d0 = int(self.dec_idx[0])
+            self.dec_bt = inp.block_table[d0:].contiguous()
+            self.dec_sl = inp.seq_lens[d0:].contiguous()
+            ws = pa.decode_workspace_size(nd, self.max_s)
+            self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+            self.dec_out = torch.empty(nd, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=device)
+            self.dec_lse = torch.empty(nd, W.HQ, dtype=torch.float32, device=device)
+        if self.n_chunk_rows:
+            self.pf_cu = inp.cu_q_lens[:2].contiguous()
+            self.pf_bt = inp.block_table[:1].contiguous()
+            self.pf_sl = inp.seq_lens[:1].contiguous()
+            self.pf_out = torch.empty(self.n_chunk_rows, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16,
+                                      device=device)
+            self.pf_lse = torch.empty(self.n_chunk_rows, W.HQ, dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.launches_per_step = self.layers * ((1 if self.append else 0) + (1 if self.n_chunk_rows else 0)
+                                                + (2 if nd else 0))
+
+    def run(self, events=None, q_src=None):
+        pa, inp = self.pa, self.inp
+        stream = torch.cuda.current_stream()
+        for layer in range(self.layers):
+            q = inp.q[layer] if q_src is None else q_src[layer]
+            if self.append:
+                pa.kv_append_paged(inp.k_new[layer], inp.v_new[layer], inp.cu_q_lens, inp.start_pos,
+                                   inp.block_table, inp.k_pools[layer], inp.v_pools[layer],
+                                   status=self.status, stream=stream)
+            if self.n_chunk_rows:
+                if events is not None:
+                    events["pf"][layer][0].record(stream)
+                pa.attn_prefill_chunk(q[:self.n_chunk_rows], self.pf_cu, inp.k_pools[layer],
+                                      inp.v_pools[layer], self.pf_bt, self.pf_sl, self.n_chunk_rows,
+                                      self.max_s, inp.scale, out=self.pf_out, lse=self.pf_lse,
+                                      status=self.status, stream=stream)
+                if events is not None:
+                    events["pf"][layer][1].record(stream)
+            if len(self.dec_idx):
+                if events is not None:
+                    events["dec"][layer][0].record(stream)
+                pa.attn_decode_paged(q[self.n_chunk_rows:], inp.k_pools[layer], inp.v_pools[layer],
+                                     self.dec_bt, self.dec_sl, self.max_s, inp.scale,
+                                     out=self.dec_out, lse=self.dec_lse, workspace=self.ws,
+                                     status=self.status, stream=stream)
+                if events is not None:
+                    events["dec"][layer][1].record(stream)
+
+
+def make_events(layers):
+    mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(layers)]
+    return {"pf": mk(), "dec": mk()}
+
+
+def elapsed(evs):
+    return sum(a.elapsed_time(b) for a, b in evs) / 1e3  # seconds
+
+
+# ----------------------------------------------------------------------------------------------
+# end-to-end through the public calls with host buffers
+# ----------------------------------------------------------------------------------------------
+def e2e_run(step: Step, steps: int):
+    """Per step and layer: H2D of q, k_new, v_new (pinned), the four calls, D2H of every output.
+
+    Decode e2e time per layer spans its q H2D, the decode call and the D2H of its output; the
+    prefill phase likewise. Returns (decode GB/s, prefill TFLOP/s, h2d bytes, d2h bytes)."""
+    inp = step.inp
+    L = step.layers
+    host_q = [inp.q[l].cpu().pin_memory() for l in range(L)]
+    host_k = [inp.k_new[l].cpu().pin_memory() for l in range(L)] if step.append else None
+    host_v = [inp.v_new[l].cpu().pin_memory() for l in range(L)] if step.append else None
+    dev_q = torch.empty_like(inp.q[0])
+    dev_k = torch.empty_like(inp.k_new[0]) if step.append else None
+    dev_v = torch.empty_like(inp.v_new[0]) if step.append else None
+    out_pf = torch.empty((max(step.n_chunk_rows, 1), W.HQ, W.HEAD_DIM), dtype=torch.bfloat16).pin_memory()
+    lse_pf = torch.empty((max(step.n_chunk_rows, 1), W.HQ), dtype=torch.float32).pin_memory()
+    nd = len(step.dec_idx)
+    out_dec = torch.empty((max(nd, 1), W.HQ, W.HEAD_DIM), dtype=torch.bfloat16).pin_memory()
+    lse_dec = torch.empty((max(nd, 1), W.HQ), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    pa = step.pa
+    h2d = d2h = 0
+    t_dec = t_pf = 0.0
+    torch.cuda.synchronize()
+    meta_host = [t.cpu().pin_memory() for t in (inp.cu_q_lens, inp.start_pos, inp.seq_lens)]
+    meta_dev = [inp.cu_q_lens, inp.start_pos, inp.seq_lens]
+    for s in range(steps):
+        ev = make_events(L)
+        for hsrc, ddst in zip(meta_host, meta_dev):   # the step's lengths and positions
+            ddst.copy_(hsrc, non_blocking=True)
+            if s == 0:
+                h2d += hsrc.numel() * 4
+        for layer in range(L):
+            if step.append:
+                dev_k.copy_(host_k[layer], non_blocking=True)
+                dev_v.copy_(host_v[layer], non_blocking=True)
+                pa.kv_append_paged(dev_k, dev_v, inp.cu_q_lens, inp.start_pos, inp.block_table,
+                                   inp.k_pools[layer], inp.v_pools[layer], stream=stream)
+                if s == 0:
+                    h2d += 2 * dev_k.numel() * 2
+            if step.n_chunk_rows:
+                ev["pf"][layer][0].record(stream)
+                n = step.n_chunk_rows
+                dev_q[:n].copy_(host_q[layer][:n], non_blocking=True)
+                pa.attn_prefill_chunk(dev_q[:n], step.pf_cu, inp.k_pools[layer], inp.v_pools[layer],
+                                      step.pf_bt, step.pf_sl, n, step.max_s, inp.scale,
+                                      out=step.pf_out, lse=step.pf_lse, stream=stream)
+                out_pf.copy_(step.pf_out, non_blocking=True)
+                lse_pf.copy_(step.pf_lse, non_blocking=True)
+                ev["pf"][layer][1].record(stream)
+                if s == 0:
+                    h2d += n * W.HQ * W.HEAD_DIM * 2
+                    d2h += out_pf.numel() * 2 + lse_pf.numel() * 4
+            if nd:
+                ev["dec"][layer][0].record(stream)
+                n0 = step.n_chunk_rows
+                dev_q[n0:n0 + nd].copy_(host_q[layer][n0:n0 + nd], non_blocking=True)
+                pa.attn_decode_paged(dev_q[n0:n0 + nd], inp.k_pools[layer], inp.v_pools[layer],
+                                     step.dec_bt, step.dec_sl, step.max_s, inp.scale,
+                                     out=step.dec_out, lse=step.dec_lse, workspace=step.ws,
+                                     stream=stream)
+                out_dec.copy_(step.dec_out, non_blocking=True)
+                lse_dec.copy_(step.dec_lse, non_blocking=True)
+                ev["dec"][layer][1].record(stream)
+                if s == 0:
+                    h2d += nd * W.HQ * W.HEAD_DIM * 2
+                    d2h += out_dec.numel() * 2 + lse_dec.numel() * 4
+        torch.cuda.synchronize()
+        if nd:
+            t_dec += elapsed(ev["dec"])
+        if step.n_chunk_rows:
+            t_pf += elapsed(ev["pf"])
+    dec = step.dec_bytes * L * steps / t_dec / 1e9 if nd else None
+    pf = step.pf_flops * L * steps / t_pf / 1e12 if step.n_chunk_rows else None
+    return dec, pf, h2d, d2h
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ----------------------------------------------------------------------------------------------
+def cpu_baseline(step: Step, budget_s: float = 12.0):
+    import oracle
+    inp = step.inp
+    cores = len(os.sched_getaffinity(0))
+    kp = inp.k_pools[0].view(torch.int16).cpu().numpy()
+    vp = inp.v_pools[0].view(torch.int16).cpu().numpy()
+    q = inp.q[0].view(torch.int16).cpu().numpy()
+    res = {}
+    if len(step.dec_idx):
+        n0 = step.n_chunk_rows
+        bt = inp.host_block_table[len(step.chunk_idx):]
+        sl = inp.host_seq_lens[len(step.chunk_idx):]
+        t0 = time.perf_counter()
+        done = 0
+        seqs = []
+        for b in range(len(sl)):
+            oracle.decode(q[n0:], kp, vp, bt, sl, inp.scale, seqs=[b], threads=cores)
+            done += int(sl[b])
+            seqs.append(b)
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        res["decode"] = {"value": done * W.kv_bytes_per_token() / dt / 1e9, "unit": "GB/s",
+                         "sample": f"oracle decode of {len(seqs)} of {len(sl)} sequences of layer 0 "
+                                   f"({done} cached tokens), {dt:.1f} s"}
+    if step.n_chunk_rows:
+        n = step.n_chunk_rows
+        L0 = int(inp.host_seq_lens[0])
+        rows = list(range(n - 64, n))
+        t0 = time.perf_counter()
+        oracle.prefill(q[:n], [0, n], kp, vp, inp.host_block_table[:1], inp.host_seq_lens[:1],
+                       inp.scale, rows=rows, threads=cores)
+        dt = time.perf_counter() - t0
+        pairs = sum(L0 - n + r + 1 for r in rows)
+        res["prefill"] = {"value": prefill_flops(pairs) / dt / 1e12, "unit": "TFLOP/s",
+                          "sample": f"oracle prefill of the last 64 chunk rows x 16 heads of layer 0, {dt:.1f} s"}
+    return res, cores
+
+
+# ----------------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="mixed_28l", choices=sorted(W.CONFIG_SEED))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clocks-out", default=None)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import long_context_paged_gb300 as pa
+    pa.load()
+    dev = f"cuda:{local}"
+    step = Step(pa, args.workload, dev)
+    hbm, bf16, bf16s, peak_src = peaks()
+
+    for _ in range(max(args.warmup, 0)):
+        step.run()
+    torch.cuda.synchronize()
+    flags = pa.read_device_status(step.status)
+    if flags:
+        raise RuntimeError(f"device status flagged errors during warm-up: {flags}")
+
+    sampler = ClockSampler(args.clocks_out)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    all_ev = []
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        ev = make_events(step.layers)
+        step.run(events=ev)
+        all_ev.append(ev)
+    stop.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop(device_uuid()) if rank == 0 else None
+
+    total_s = start.elapsed_time(stop) / 1e3
+    t_dec = sum(elapsed(e["dec"]) for e in all_ev) if len(step.dec_idx) else 0.0
+    t_pf = sum(elapsed(e["pf"]) for e in all_ev) if step.n_chunk_rows else 0.0
+    if dist is not None:
+        t = torch.tensor([total_s, t_dec, t_pf], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s, t_dec, t_pf = t.tolist()
+    n = world
+    launches = step.launches_per_step * args.steps
+    dec_gbs = step.dec_bytes * step.layers * args.steps * n / t_dec / 1e9 if t_dec else None
+    pf_tflops = step.pf_flops * step.layers * args.steps * n / t_pf / 1e12 if t_pf else None
+
+    if pa.read_device_status(step.status):
+        raise RuntimeError("device status flagged errors in the timed region")
+
+    e2e = None
+    if not args.no_e2e:
+        e_dec, e_pf, h2d, d2h = e2e_run(step, max(1, min(args.steps, 3)))
+        e2e = {"value": None if e_dec is None else round(e_dec * n, 1), "unit": "GB/s",
+               "prefill_value": None if e_pf is None else round(e_pf * n, 2),
+               "prefill_unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        res, cores = cpu_baseline(step)
+        main_key = "decode" if "decode" in res else "prefill"
+        cpu = {"value": round(res[main_key]["value"], 4), "unit": res[main_key]["unit"],
+               "cores": cores, "kind": "oracle", "sample": res[main_key]["sample"]}
+        if main_key == "decode" and "prefill" in res:
+            cpu["prefill"] = {"value": round(res["prefill"]["value"], 5), "unit": "TFLOP/s",
+                              "sample": res["prefill"]["sample"]}
+
+    # roofline of the dominant kernel (by device time), the other one alongside
+    dec_src = source_hash("decode.cu", "pa_common.cuh")
+    pf_src = source_hash("prefill.cu", "pa_common.cuh")
+    roofs = []
+    if t_dec:
+        per_launch_s = t_dec / (step.layers * args.steps)
+        ach = step.dec_bytes / per_launch_s / 1e9
+        roofs.append((t_dec, {"kernel": "attn_decode_paged (decode_splitkv + merge)", "bound": "hbm",
+                              "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                              "frac": round(ach / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
+                              "traffic": traffic_from_profile("decode_splitkv_mixed_28l.md", dec_src),
+                              "algorithmic_bytes_per_launch": step.dec_bytes}))
+    if t_pf:
+        per_launch_s = t_pf / (step.layers * args.steps)
+        ach = step.pf_flops / per_launch_s / 1e12
+        pk = bf16s if step.layers > 1 else bf16
+        roofs.append((t_pf, {"kernel": "attn_prefill_chunk", "bound": "tensor",
+                             "achieved": round(ach, 2), "peak": pk, "unit": "TFLOP/s",
+                             "frac": round(ach / pk, 4),
+                             "peak_source": f"{peak_src} bf16_tflops" + ("_sustained" if step.layers > 1 else ""),
+                             "traffic": traffic_from_profile("prefill_mixed_28l.md", pf_src),
+                             "algorithmic_flops_per_launch": step.pf_flops}))
+    roofs.sort(key=lambda x: -x[0])
+
+    L = step.inp.host_seq_lens
+    value = dec_gbs if dec_gbs is not None else pf_tflops
+    unit = "GB/s" if dec_gbs is not None else "TFLOP/s"
+    line = {
+        "metric": "paged GQA attn: decode KV-read GB/s (% HBM peak); prefill-chunk TFLOP/s (% peak)",
+        "value": round(value, 2), "unit": unit, "n_gpus": n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, paged 16, scattered pages)",
+        "config": {"workload": args.workload, "layers": step.layers,
+                   "decode_seqs": int(len(step.dec_idx)),
+                   "decode_kv_tokens": int(L[step.dec_idx].sum()) if len(step.dec_idx) else 0,
+                   "prefill_chunk": step.n_chunk_rows,
+                   "prefill_offset": int(L[0] - step.n_chunk_rows) if step.n_chunk_rows else None,
+                   "heads": "16q/8kv", "head_dim": 128, "page_size": 16,
+                   "parallelism": f"replicas x{n}",
+                   "l2": "inputs larger than L2 (each step reads every layer's pools)"},
+        "decode": None if dec_gbs is None else {"value": round(dec_gbs, 1), "unit": "GB/s",
+                                                 "frac_of_hbm_peak": round(dec_gbs / hbm, 4)},
+        "prefill": None if pf_tflops is None else {"value": round(pf_tflops, 2), "unit": "TFLOP/s",
+                                                    "frac_of_bf16_peak": round(pf_tflops / (bf16s if step.layers > 1 else bf16), 4)},
+        "roofline": roofs[0][1] if roofs else None,
+        "roofline_other": [r[1] for r in roofs[1:]],
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16s,
+                  "source": peak_src},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle  # noqa: F401
+    name = args.workload
+    L, ql = W.lengths_for(name)
+    # only the data the sampled work touches is generated (on the host)
+    cores = len(os.sched_getaffinity(0))
+    inp = W.make_workload(name, device="cpu", layers=1) if name != "mixed_28l" else \
+        W.make_paged(W.CONFIG_SEED[name], L, ql, pool_factor=1.0, extra_pages=16, layers=1)
+    step = type("S", (), {})()
+    step.inp = inp
+    is_chunk = inp.host_q_lens > 1
+    step.chunk_idx = np.nonzero(is_chunk)[0]
+    step.dec_idx = np.nonzero(~is_chunk)[0]
+    step.n_chunk_rows = int(inp.host_q_lens[step.chunk_idx].sum()) if len(step.chunk_idx) else 0
+    budget = max(2.0, 20.0 / max(1, args.steps + args.warmup))
+    vals, pvals = [], []
+    sample = None
+    for i in range(args.warmup + args.steps):
+        res, _ = cpu_baseline(step, budget_s=budget)
+        if i >= args.warmup:
+            k = "decode" if "decode" in res else "prefill"
+            vals.append(res[k]["value"])
+            sample = res[k]["sample"]
+            unit = res[k]["unit"]
+            if "prefill" in res and k == "decode":
+                pvals.append(res["prefill"]["value"])
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": "paged GQA attn: decode KV-read GB/s (% HBM peak); prefill-chunk TFLOP/s (% peak)",
+            "value": round(v, 4), "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": name},
+            "cpu_baseline": {"value": round(v, 4), "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "prefill": {"value": round(statistics.median(pvals), 5), "unit": "TFLOP/s"} if pvals else None,
+            "e2e": {"value": round(v, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * pagedattn.h — C ABI of the GB300 (sm_103a) paged GQA attention library.
+ *
+ * The operation is attention of a Qwen3-style text decoder (GQA: 16 query heads share 8 KV
+ * heads, head_dim 128) over a paged KV cache holding tens of thousands of audio-embedding
+ * tokens, in its two modes:
+ *   - decode: one query row per sequence against the sequence's whole cache
+ *     ("Optimizing ASR Models to Transcribe 90-Minute Multi-Speaker Audio", section
+ *     "Where Time Is Spent: Profiling": the autoregressive decode loop takes more than 94% of
+ *     the time on long audio);
+ *   - chunked prefill: a chunk of up to 4096 query rows attends causally to the cached prefix
+ *     plus itself (same page, section "Chunked Prefill for Long Audio"; "MOSS-Transcribe-
+ *     Diarize" cookbook, section "Inference Pipeline").
+ * The new tokens' K/V are written into the cache before attention (prefill "builds its KV
+ * cache": first page, section "ASR Model Primer").
+ *
+ * Definition (for every query row, query head h, visible keys t):
+ *     s_t = scale * <q_h, k_t>,  o_h = sum_t softmax(s)_t v_t,  lse_h = ln sum_t exp(s_t)
+ * where k_t, v_t are KV head h / (Hq / Hkv) of token t.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor arguments are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or keeps them. Scratch ("workspace") memory is caller-provided too.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream). The
+ *    host never waits for the GPU inside a call, and grids depend only on host arguments,
+ *    so calls may be captured in a CUDA graph.
+ *  - Argument errors are returned synchronously, before anything is launched.
+ *  - Errors that only the GPU can see (a block-table entry outside the pool, a length that
+ *    does not fit the block table, a bounded wait that gave up) are OR-ed as PA_DEV_* bits
+ *    into `*status`, a caller-owned device int32 (may be NULL: then they are not reported).
+ *    The kernel then skips the offending access (page 0 is read instead of an out-of-range
+ *    page, a too-long sequence is cut to what its table row covers), so no access ever
+ *    leaves the buffers described below.
+ *  - Supported shape: bf16 storage, head_dim 128, page_size 16, num_kv_heads 8,
+ *    num_q_heads 16 (the decoder's GQA 16/8). Anything else returns PA_ERR_UNSUPPORTED.
+ *
+ * Layouts (row-major, contiguous, little-endian)
+ *  - KV page pool (one K pool and one V pool per layer): bf16 [num_pages][16][Hkv][128].
+ *    Token position p of sequence b lives in page block_table[b * bt_stride + p / 16],
+ *    slot p % 16.
+ *  - block_table: int32 [batch][bt_stride]; entries past ceil(seq_len / 16) are never read.
+ *  - q and out: bf16 [rows][Hq][128]; lse: fp32 [rows][Hq] (natural log), may be NULL.
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,         /* null pointer, negative size, inconsistent sizes        */
+  PA_ERR_UNSUPPORTED = 2,         /* head counts, head_dim or page size not supported        */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the matching *_workspace_size()  */
+  PA_ERR_CUDA = 4                 /* a CUDA runtime call failed; see pa_last_error()         */
+} pa_status;
+
+/* Device-side error bits, OR-ed into the optional `status` word. */
+#define PA_DEV_ERR_PAGE_OOB 1u /* a block-table entry needed by the call was not in [0, num_pages) */
+#define PA_DEV_ERR_LENGTH 2u   /* a length did not fit: seq_len < 0 or > bt_stride*16, q_len > seq_len, ... */
+#define PA_DEV_ERR_TIMEOUT 4u  /* a bounded wait inside a kernel gave up (the kernel returned early) */
+
+typedef struct pa_dims {
+  int32_t num_q_heads;  /* Hq  (16) */
+  int32_t num_kv_heads; /* Hkv (8)  */
+  int32_t head_dim;     /* D   (128) */
+  int32_t page_size;    /* tokens per page (16) */
+} pa_dims;
+
+/* ------------------------------------------------------------------------------------------
+ * kv_append_paged — write the K/V rows of new tokens into the page pools.
+ *
+ * Source: prefill builds the KV cache and decode extends it by one token per step
+ * ("Optimizing ASR Models to Transcribe 90-Minute Multi-Speaker Audio", section "ASR Model
+ * Primer"; chunked prefill appends 4096 tokens per step, section "Chunked Prefill for Long
+ * Audio").
+ *
+ *   k_new, v_new   bf16 [total_new][Hkv][128], new tokens packed by sequence
+ *   cu_new_lens    int32 [batch+1]: sequence b owns rows cu_new_lens[b] .. cu_new_lens[b+1]-1
+ *   start_pos      int32 [batch]: logical position of sequence b's first new token
+ *   block_table    int32 [batch][bt_stride]; must already cover the new positions
+ *   k_pool, v_pool bf16 [num_pages][16][Hkv][128], written in place
+ * Row j of sequence b goes to position start_pos[b] + j. The copy is bit-exact; no other
+ * pool byte changes. Rows at or past cu_new_lens[batch] are ignored. A position whose table
+ * entry is missing (past bt_stride) or out of range is skipped and flagged.
+ * ------------------------------------------------------------------------------------------ */
+pa_status kv_append_paged(pa_dims dims, const void* k_new, const void* v_new, int32_t total_new,
+                          const int32_t* cu_new_lens, const int32_t* start_pos, int32_t batch,
+                          const int32_t* block_table, int32_t bt_stride, void* k_pool,
+                          void* v_pool, int64_t num_pages, int32_t* status, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * attn_decode_paged — one decode step: query row b attends to all seq_lens[b] cached keys.
+ *
+ * Source: the autoregressive decode of the transcript, one token at a time against the KV
+ * cache ("MOSS-Transcribe-Diarize" cookbook, "Inference Pipeline" item 3; dominant share
+ * of time per "Where Time Is Spent" on both the blog and the cookbook).
+ *
+ *   q            bf16 [batch][Hq][128]
+ *   seq_lens     int32 [batch], keys per sequence (0 allowed: o = 0, lse = -inf)
+ *   max_seq_len  host upper bound of seq_lens (<= 131072, the 128K context); a larger
+ *                device value is cut to bt_stride*16 and flagged
+ *   out          bf16 [batch][Hq][128];  lse fp32 [batch][Hq] or NULL
+ *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes, 256-byte
+ *                aligned; holds per-split partial results. Calls that share a workspace must
+ *                not overlap on the GPU.
+ * The key range of all sequences is cut into equal page ranges, one per resident CTA
+ * (split-KV); partial (o, lse) pairs of sequences that span ranges are merged by log-sum-exp.
+ * ------------------------------------------------------------------------------------------ */
+size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len);
+
+pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool, const void* v_pool,
+                            int64_t num_pages, const int32_t* block_table, int32_t bt_stride,
+                            const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                            float softmax_scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, int32_t* status, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * attn_prefill_chunk — causal attention of query chunks over their cached prefix + themselves.
+ *
+ * Source: chunked prefill of long audio prompts in 4096-token pieces ("Optimizing ASR Models
+ * to Transcribe 90-Minute Multi-Speaker Audio", section "Chunked Prefill for Long Audio").
+ *
+ *   q           bf16 [total_q][Hq][128], chunks packed by sequence
+ *   cu_q_lens   int32 [batch+1]: chunk b owns rows cu_q_lens[b] .. cu_q_lens[b+1]-1
+ *   seq_lens    int32 [batch]: keys of sequence b INCLUDING the chunk (appended first)
+ *   max_q_len   host upper bound of the chunk lengths (grid size)
+ * Query i of chunk b (length n) sits at position seq_lens[b] - n + i and sees keys
+ * 0 .. seq_lens[b] - n + i (bottom-right causal alignment). A chunk longer than its sequence
+ * is flagged and produces nothing.
+ *   out bf16 [total_q][Hq][128]; lse fp32 [total_q][Hq] or NULL.
+ *   workspace: pa_prefill_workspace_size(...) bytes (may be 0 / NULL when that is 0).
+ * ------------------------------------------------------------------------------------------ */
+size_t pa_prefill_workspace_size(pa_dims dims, int32_t batch, int32_t max_q_len,
+                                 int32_t max_seq_len);
+
+pa_status attn_prefill_chunk(pa_dims dims, const void* q, const int32_t* cu_q_lens,
+                             int32_t total_q, const void* k_pool, const void* v_pool,
+                             int64_t num_pages, const int32_t* block_table, int32_t bt_stride,
+                             const int32_t* seq_lens, int32_t batch, int32_t max_q_len,
+                             int32_t max_seq_len, float softmax_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, int32_t* status,
+                             pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * attn_merge_lse — combine attention results computed over disjoint key sets.
+ *
+ * Source: the split-KV form of the decode step (long caches are cut into key ranges whose
+ * softmax states are merged exactly): with lse = ln sum_s exp(lse_s),
+ *     o = sum_s exp(lse_s - lse) * o_s.
+ * Parts with lse_s = -inf carry no weight (their o_s is never read); if all parts are empty
+ * the result is o = 0, lse = -inf.
+ *
+ *   o_parts    fp32 [num_parts][rows][heads][head_dim], each part normalised on its own
+ *   lse_parts  fp32 [num_parts][rows][heads]
+ *   out        bf16 [rows][heads][head_dim];  lse_out fp32 [rows][heads] or NULL
+ * head_dim must be a multiple of 4 (<= 1024).
+ * ------------------------------------------------------------------------------------------ */
+pa_status attn_merge_lse(int32_t num_parts, int32_t rows, int32_t heads, int32_t head_dim,
+                         const float* o_parts, const float* lse_parts, void* out,
+                         float* lse_out, pa_stream_t stream);
+
+/* Read and clear the device status word: waits for `stream`, copies *status to *flags_out,
+ * then zeroes it. */
+pa_status pa_read_device_status(int32_t* status, uint32_t* flags_out, pa_stream_t stream);
+
+/* Static text for a status code. */
+const char* pa_status_string(pa_status s);
+
+/* Text of the last CUDA error seen by a call of the calling host thread ("" if none). */
+const char* pa_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

@@ -1,0 +1,237 @@
+"""GB300-native paged GQA attention: Python binding of ``libpagedattn.so``.
+
+Thin ctypes marshalling over the C ABI in ``include/pagedattn.h``: every computation runs in
+the library's CUDA kernels. PyTorch only provides device memory and streams. There is no CPU
+or fallback path: if the shared library has not been built, ``load()`` raises.
+
+Calls (same names as the C ABI):
+
+* ``kv_append_paged``   write new tokens' K/V rows into their page slots
+* ``attn_decode_paged`` one decode step over a paged KV cache (split-KV + log-sum-exp merge)
+* ``attn_prefill_chunk`` causal attention of query chunks over their cached prefix + themselves
+* ``attn_merge_lse``    combine partial results over disjoint key sets
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "load", "PagedAttnError", "Dims", "DEFAULT_DIMS",
+    "kv_append_paged", "attn_decode_paged", "attn_prefill_chunk", "attn_merge_lse",
+    "decode_workspace_size", "prefill_workspace_size", "read_device_status",
+    "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "lib_path",
+]
+
+DEV_ERR_PAGE_OOB = 1
+DEV_ERR_LENGTH = 2
+DEV_ERR_TIMEOUT = 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "_lib", "libpagedattn.so")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32)]
+
+
+DEFAULT_DIMS = (16, 8, 128, 16)
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        lib = load()
+        text = lib.pa_status_string(code).decode()
+        detail = lib.pa_last_error().decode()
+        super().__init__(f"{call} failed: {text} ({code}){': ' + detail if detail else ''}")
+        self.code = code
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+_SIGS = {
+    "kv_append_paged": (_I32, [Dims, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _I64, _P, _P]),
+    "pa_decode_workspace_size": (_SZ, [Dims, _I32, _I32]),
+    "attn_decode_paged": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _P, _P, _P,
+                                 _SZ, _P, _P]),
+    "pa_prefill_workspace_size": (_SZ, [Dims, _I32, _I32, _I32]),
+    "attn_prefill_chunk": (_I32, [Dims, _P, _P, _I32, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
+                                  _F, _P, _P, _P, _SZ, _P, _P]),
+    "attn_merge_lse": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "pa_read_device_status": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
+    "pa_status_string": (ctypes.c_char_p, [_I32]),
+    "pa_last_error": (ctypes.c_char_p, []),
+    "pa_version": (_I32, []),
+}
+
+
+def load():
+    """Load the built library (raises if it is missing: there is no fallback)."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+# ----------------------------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------------------------
+def _dims(dims):
+    return Dims(*(dims or DEFAULT_DIMS))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _check(call, code):
+    if code != 0:
+        raise PagedAttnError(call, code)
+
+
+# ----------------------------------------------------------------------------------------------
+# the four calls
+# ----------------------------------------------------------------------------------------------
+def kv_append_paged(k_new, v_new, cu_new_lens, start_pos, block_table, k_pool, v_pool, *,
+                    status=None, stream=None, dims=None):
+    """Write rows of k_new/v_new [T, Hkv, D] into the pools at their block-table slots."""
+    for t, n, d in ((k_new, "k_new", torch.bfloat16), (v_new, "v_new", torch.bfloat16),
+                    (cu_new_lens, "cu_new_lens", torch.int32), (start_pos, "start_pos", torch.int32),
+                    (block_table, "block_table", torch.int32), (k_pool, "k_pool", torch.bfloat16),
+                    (v_pool, "v_pool", torch.bfloat16)):
+        _need(t, n, d)
+    lib = load()
+    _check("kv_append_paged", lib.kv_append_paged(
+        _dims(dims), _ptr(k_new), _ptr(v_new), k_new.shape[0], _ptr(cu_new_lens), _ptr(start_pos),
+        start_pos.shape[0], _ptr(block_table), block_table.shape[1], _ptr(k_pool), _ptr(v_pool),
+        k_pool.shape[0], _ptr(status), _stream(stream)))
+
+
+def decode_workspace_size(batch: int, max_seq_len: int, dims=None) -> int:
+    return int(load().pa_decode_workspace_size(_dims(dims), batch, max_seq_len))
+
+
+def prefill_workspace_size(batch: int, max_q_len: int, max_seq_len: int, dims=None) -> int:
+    return int(load().pa_prefill_workspace_size(_dims(dims), batch, max_q_len, max_seq_len))
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is not None:
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int,
+                      softmax_scale: float, *, out=None, lse=None, workspace=None, status=None,
+                      stream=None, want_lse=True, dims=None):
+    """Decode attention: q [B, Hq, D] over each sequence's cached keys. Returns (out, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(B, q.shape[1], dtype=torch.float32, device=q.device)
+    ws_bytes = decode_workspace_size(B, max_seq_len, dims)
+    workspace = _workspace(ws_bytes, q.device, workspace)
+    lib = load()
+    _check("attn_decode_paged", lib.attn_decode_paged(
+        _dims(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), float(softmax_scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
+    return out, lse
+
+
+def attn_prefill_chunk(q, cu_q_lens, k_pool, v_pool, block_table, seq_lens, max_q_len: int,
+                       max_seq_len: int, softmax_scale: float, *, out=None, lse=None,
+                       workspace=None, status=None, stream=None, want_lse=True, dims=None):
+    """Chunked prefill: q [Tq, Hq, D] packed by cu_q_lens. Returns (out, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    ws_bytes = prefill_workspace_size(B, max_q_len, max_seq_len, dims)
+    if ws_bytes > 0:
+        workspace = _workspace(ws_bytes, q.device, workspace)
+    lib = load()
+    _check("attn_prefill_chunk", lib.attn_prefill_chunk(
+        _dims(dims), _ptr(q), _ptr(cu_q_lens), q.shape[0], _ptr(k_pool), _ptr(v_pool),
+        k_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+        int(max_q_len), int(max_seq_len), float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
+    return out, lse
+
+
+def attn_merge_lse(o_parts, lse_parts, *, out=None, lse_out=None, stream=None):
+    """o_parts fp32 [S, R, H, D], lse_parts fp32 [S, R, H] -> (out bf16 [R, H, D], lse [R, H])."""
+    _need(o_parts, "o_parts", torch.float32, 4)
+    _need(lse_parts, "lse_parts", torch.float32, 3)
+    S, R, H, D = o_parts.shape
+    if out is None:
+        out = torch.empty(R, H, D, dtype=torch.bfloat16, device=o_parts.device)
+    if lse_out is None:
+        lse_out = torch.empty(R, H, dtype=torch.float32, device=o_parts.device)
+    lib = load()
+    _check("attn_merge_lse", lib.attn_merge_lse(S, R, H, D, _ptr(o_parts), _ptr(lse_parts),
+                                                _ptr(out), _ptr(lse_out), _stream(stream)))
+    return out, lse_out
+
+
+def read_device_status(status, stream=None) -> int:
+    """Wait for the stream, return the device status bits and clear them."""
+    _need(status, "status", torch.int32)
+    flags = ctypes.c_uint32(0)
+    _check("pa_read_device_status", load().pa_read_device_status(_ptr(status), ctypes.byref(flags),
+                                                                 _stream(stream)))
+    return int(flags.value)

@@ -1,0 +1,527 @@
+// attn_decode_paged: split-KV decode attention over a paged KV cache (sm_103a).
+//
+// Source: the autoregressive decode step of the Qwen3 text decoder (GQA 16/8, head_dim 128)
+// that "Optimizing ASR Models to Transcribe 90-Minute Multi-Speaker Audio" ("Where Time Is
+// Spent: Profiling") and the "MOSS-Transcribe-Diarize" cookbook ("Where Time Is Spent",
+// "Inference Pipeline" item 3) name as the dominant cost on long audio: one query token per
+// sequence reads the whole cached K/V of every layer, so the step is bound by HBM reads.
+//
+// Design (GB300):
+//  * Persistent grid, one CTA per SM. The pages of all sequences are laid end to end and cut
+//    into equal contiguous page ranges, one per CTA, so a ragged batch (375 .. 70,000 tokens)
+//    is balanced to within one page. A sequence cut by a range boundary yields one partial
+//    (o, lse) per CTA that touches it; a second small kernel merges them by log-sum-exp.
+//  * A page holds 16 tokens x 8 KV heads x 128 dims of K (32 KB, contiguous) and the same of
+//    V. A producer warp streams whole pages into a 3-stage shared-memory ring with bulk
+//    asynchronous copies (cp.async.bulk + mbarrier transaction counts): 64 KB per stage,
+//    up to 192 KB in flight per SM. Block-table entries are fetched 32 at a time.
+//  * Eight consumer warps, one per KV head; each serves BOTH query heads of its GQA group
+//    from one read of the K/V rows. Lane (c, th) holds dims 8c..8c+7 of tokens th*8..th*8+7.
+//    Scores are reduce-scattered across the 16 lanes of a half-warp (15 shuffles per page
+//    for 16 scores), so each lane ends with exactly one (token, head) score and one exp2.
+//  * fp32 math on bf16 loads, paired fp32 FMAs (fma.rn.f32x2). The running max is only moved
+//    when a page exceeds it by more than 8 (log2 units), so the accumulators are rescaled
+//    rarely; probabilities stay <= 2^8 and the result is exact up to rounding.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kConsumerWarps = kHkv;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr uint32_t kPageBytes = kPage * kHkv * kHeadDim * 2;  // K (or V) of one page
+constexpr int kMaxBatch = 4096;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct DecodeSmem {
+  uint8_t kv[kStages][2][kPageBytes];
+  float p[kConsumerWarps][32];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int32_t warp_tot[kThreads / 32];
+  int32_t total;
+  int32_t prefix[kMaxBatch + 1];
+};
+
+struct DecodeParams {
+  const uint16_t* q;
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t max_seq_len;
+  float scale_log2;
+  uint16_t* out;
+  float* lse;
+  int32_t* ws_header;  // [0] = pages per CTA (W), [1] = total pages, [2] = grid size
+  int32_t* ws_prefix;  // [batch + 1]
+  float* ws_lse;       // [records][Hq]
+  float* ws_o;         // [records][Hq][D]
+  int32_t* status;
+};
+
+// Keys of sequence b as the kernels use them: negative -> 0, more than the table row covers
+// -> cut to bt_stride * 16 (both flagged).
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, bool report) {
+  int L = p.seq_lens[b];
+  const int cap = p.bt_stride * kPage;
+  if (L < 0 || L > cap || L > p.max_seq_len) {
+    if (report) flag_error(p.status, PA_DEV_ERR_LENGTH);
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+  }
+  return L;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// prefix[b] = first global page of sequence b, prefix[batch] = total pages.
+__device__ void build_prefix(const DecodeParams& p, DecodeSmem& s) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (p.batch + kThreads - 1) / kThreads;
+  const int b0 = min(p.batch, tid * per), b1 = min(p.batch, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += (clamp_len(p, b, blockIdx.x == 0) + kPage - 1) / kPage;
+  const int incl = warp_incl_scan(local, lane);
+  if (lane == 31) s.warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < kThreads / 32 ? s.warp_tot[lane] : 0;
+    int sc = warp_incl_scan(v, lane);
+    if (lane < kThreads / 32) s.warp_tot[lane] = sc - v;
+    if (lane == 31) s.total = sc;
+  }
+  __syncthreads();
+  int run = s.warp_tot[warp] + incl - local;
+  for (int b = b0; b < b1; ++b) {
+    s.prefix[b] = run;
+    run += (clamp_len(p, b, false) + kPage - 1) / kPage;
+  }
+  if (tid == 0) s.prefix[p.batch] = s.total;
+  __syncthreads();
+}
+
+// Last b with prefix[b] <= x (prefix non-decreasing, prefix[0] = 0 <= x < prefix[batch]).
+__device__ __forceinline__ int find_seq(const int32_t* prefix, int batch, int x) {
+  int lo = 0, hi = batch;  // invariant: prefix[lo] <= x < prefix[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const DecodeParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  DecodeSmem& s = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
+
+  const int total = s.total;
+  const int W = (total + gridDim.x - 1) / gridDim.x;
+  if (blockIdx.x == 0) {
+    if (tid == 0) {
+      p.ws_header[0] = W;
+      p.ws_header[1] = total;
+      p.ws_header[2] = gridDim.x;
+    }
+    for (int b = tid; b <= p.batch; b += kThreads) p.ws_prefix[b] = s.prefix[b];
+  }
+  if (total == 0) return;
+  const int P0 = blockIdx.x * W;
+  const int P1 = min(total, P0 + W);
+  if (P0 >= P1) return;
+  const int b_first = find_seq(s.prefix, p.batch, P0);
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer warp
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int b = b_first; ok && b < p.batch && s.prefix[b] < P1; ++b) {
+      const int lp0 = max(P0, s.prefix[b]) - s.prefix[b];
+      const int lp1 = min(P1, s.prefix[b + 1]) - s.prefix[b];
+      const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+      for (int lp = lp0; ok && lp < lp1; lp += 32) {
+        const int n = min(32, lp1 - lp);
+        int entry = 0;
+        if (lane < n) {
+          entry = bt_row[lp + lane];
+          if (entry < 0 || entry >= p.num_pages) {
+            flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
+            entry = 0;
+          }
+        }
+        for (int i = 0; i < n; ++i) {
+          const int page = __shfl_sync(0xffffffffu, entry, i);
+          if (lane == 0) {
+            if (!mbar_wait_bounded(&s.empty[stage], phase ^ 1u)) {
+              flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+              ok = false;
+            } else {
+              mbar_arrive_expect_tx(&s.full[stage], 2 * kPageBytes);
+              bulk_g2s(s.kv[stage][0], p.k_pool + static_cast<int64_t>(page) * kPageBytes,
+                       kPageBytes, &s.full[stage]);
+              bulk_g2s(s.kv[stage][1], p.v_pool + static_cast<int64_t>(page) * kPageBytes,
+                       kPageBytes, &s.full[stage]);
+              ++issued;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+    // Do not leave while copies into this CTA's shared memory may still be landing.
+    if (lane == 0) {
+      int st = stage;
+      uint32_t ph = phase;
+      for (int k = 0; k < min(issued, kStages); ++k) {
+        if (--st < 0) { st = kStages - 1; ph ^= 1u; }
+        if (!mbar_wait_bounded(&s.full[st], ph)) flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumer warps
+  const int g = warp;          // KV head
+  const int c = lane & 15;     // dims 8c .. 8c+7
+  const int th = lane >> 4;    // tokens th*8 .. th*8+7 of each page
+  const bool hi_head = (c & 8) != 0;  // head of the score this lane owns after the scatter
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int b = b_first; b < p.batch && s.prefix[b] < P1; ++b) {
+    const int n_pages = s.prefix[b + 1] - s.prefix[b];
+    const int lp0 = max(P0, s.prefix[b]) - s.prefix[b];
+    const int lp1 = min(P1, s.prefix[b + 1]) - s.prefix[b];
+    if (lp0 >= lp1) continue;
+    const int L = clamp_len(p, b, false);
+
+    float2 qa[4], qb[4];
+    {
+      const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHq + 2 * g) * kHeadDim + 8 * c;
+      const uint4 ra = *reinterpret_cast<const uint4*>(qrow);
+      const uint4 rb = *reinterpret_cast<const uint4*>(qrow + kHeadDim);
+      const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qa[i] = make_float2(bf16lo(wa[i]) * p.scale_log2, bf16hi(wa[i]) * p.scale_log2);
+        qb[i] = make_float2(bf16lo(wb[i]) * p.scale_log2, bf16hi(wb[i]) * p.scale_log2);
+      }
+    }
+    float2 acc_a[4], acc_b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc_a[i] = acc_b[i] = make_float2(0.f, 0.f);
+    float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F;  // max used for the exponent, per head
+    float l_part = 0.f;                               // this lane's share of its head's sum
+
+    bool all_ok = true;
+    for (int lp = lp0; lp < lp1; ++lp) {
+      const int n_valid = min(kPage, L - lp * kPage);
+      bool ok = true;
+      if (!mbar_wait_bounded(&s.full[stage], phase)) {
+        flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) {
+        all_ok = false;
+        break;
+      }
+      const uint8_t* Ks = s.kv[stage][0] + g * (kHeadDim * 2) + c * 16;
+      const uint8_t* Vs = s.kv[stage][1] + g * (kHeadDim * 2) + c * 16;
+
+      // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 kr = lds128(Ks + (th * 8 + j) * (kHkv * kHeadDim * 2));
+        const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
+        const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
+        const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
+        const float2 k3 = make_float2(bf16lo(kr.w), bf16hi(kr.w));
+        float2 sa = mul2(qa[0], k0), sb = mul2(qb[0], k0);
+        sa = fma2(qa[1], k1, sa); sb = fma2(qb[1], k1, sb);
+        sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
+        sa = fma2(qa[3], k3, sa); sb = fma2(qb[3], k3, sb);
+        v[j] = sa.x + sa.y;
+        v[8 + j] = sb.x + sb.y;
+      }
+      // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score
+      //      of token th*8 + (c & 7), head (c >> 3).
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1) {
+        const bool up = (c & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+          const float send = up ? v[i] : v[w + i];
+          const float keep = up ? v[w + i] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+      }
+      float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
+
+      // ---- page max per head, lazily moved running max
+      float pm = sc;
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+      const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
+      const float pmax_a = hi_head ? pm_other : pm;
+      const float pmax_b = hi_head ? pm : pm_other;
+      if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
+        const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
+        const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
+        const float al_b = (m_b == -CUDART_INF_F) ? 0.f : fast_exp2(m_b - nb);
+        const float2 fa = make_float2(al_a, al_a), fb = make_float2(al_b, al_b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc_a[i] = mul2(acc_a[i], fa);
+          acc_b[i] = mul2(acc_b[i], fb);
+        }
+        l_part *= hi_head ? al_b : al_a;
+        m_a = na;
+        m_b = nb;
+      }
+      const float pr = fast_exp2(sc - (hi_head ? m_b : m_a));
+      l_part += pr;
+
+      // ---- hand probabilities to the lanes that own the V dims
+      s.p[warp][lane] = pr;
+      __syncwarp();
+      const float4 pa0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 0]);
+      const float4 pa1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 4]);
+      const float4 pb0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 8]);
+      const float4 pb1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 12]);
+      const float pav[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
+      const float pbv[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
+
+      // ---- o += p v over this lane's 8 tokens (invalid slots of a partial page skipped)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (th * 8 + j < n_valid) {
+          const uint4 vr = lds128(Vs + (th * 8 + j) * (kHkv * kHeadDim * 2));
+          const float2 ppa = make_float2(pav[j], pav[j]);
+          const float2 ppb = make_float2(pbv[j], pbv[j]);
+          const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
+          const float2 v1 = make_float2(bf16lo(vr.y), bf16hi(vr.y));
+          const float2 v2 = make_float2(bf16lo(vr.z), bf16hi(vr.z));
+          const float2 v3 = make_float2(bf16lo(vr.w), bf16hi(vr.w));
+          acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
+          acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
+          acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
+          acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[stage]);
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+    if (!all_ok) return;
+
+    // ---- finish this (sequence, range): denominators and the two token halves
+    float l_m = l_part;
+    l_m += __shfl_xor_sync(0xffffffffu, l_m, 1);
+    l_m += __shfl_xor_sync(0xffffffffu, l_m, 2);
+    l_m += __shfl_xor_sync(0xffffffffu, l_m, 4);
+    l_m += __shfl_xor_sync(0xffffffffu, l_m, 16);
+    const float l_o = __shfl_xor_sync(0xffffffffu, l_m, 8);
+    const float l_a = hi_head ? l_o : l_m;
+    const float l_b = hi_head ? l_m : l_o;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc_a[i].x += __shfl_xor_sync(0xffffffffu, acc_a[i].x, 16);
+      acc_a[i].y += __shfl_xor_sync(0xffffffffu, acc_a[i].y, 16);
+      acc_b[i].x += __shfl_xor_sync(0xffffffffu, acc_b[i].x, 16);
+      acc_b[i].y += __shfl_xor_sync(0xffffffffu, acc_b[i].y, 16);
+    }
+    // lanes 0..15 finish head 2g, lanes 16..31 head 2g+1
+    const int head = 2 * g + th;
+    const float l_h = th ? l_b : l_a;
+    const float m_h = th ? m_b : m_a;
+    const float inv = 1.0f / l_h;
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = th ? acc_b[i] : acc_a[i];
+      o[2 * i] = a.x * inv;
+      o[2 * i + 1] = a.y * inv;
+    }
+    const float lse_h = (m_h + log2f(l_h)) * kLn2;
+    if (lp0 == 0 && lp1 == n_pages) {
+      uint4 w;
+      w.x = pack_bf16x2(o[0], o[1]);
+      w.y = pack_bf16x2(o[2], o[3]);
+      w.z = pack_bf16x2(o[4], o[5]);
+      w.w = pack_bf16x2(o[6], o[7]);
+      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + head) * kHeadDim + 8 * c) = w;
+      if (c == 0 && p.lse != nullptr) p.lse[b * kHq + head] = lse_h;
+    } else {
+      const int64_t r = static_cast<int64_t>(b) + blockIdx.x;
+      float* dst = p.ws_o + (r * kHq + head) * kHeadDim + 8 * c;
+      reinterpret_cast<float4*>(dst)[0] = make_float4(o[0], o[1], o[2], o[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(o[4], o[5], o[6], o[7]);
+      if (c == 0) p.ws_lse[r * kHq + head] = lse_h;
+    }
+  }
+}
+
+// Merge the partial results of sequences that crossed a CTA range boundary; also writes the
+// result of empty sequences (o = 0, lse = -inf). One CTA per sequence, one warp per head.
+__global__ void __launch_bounds__(kHq * 32) decode_merge_kernel(const DecodeParams p) {
+  const int b = blockIdx.x;
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p0 = p.ws_prefix[b], p1 = p.ws_prefix[b + 1];
+  uint16_t* orow = p.out + (static_cast<int64_t>(b) * kHq + h) * kHeadDim + 4 * lane;
+  if (p1 == p0) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+    if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = -CUDART_INF_F;
+    return;
+  }
+  const int W = p.ws_header[0];
+  const int c0 = p0 / W, c1 = (p1 - 1) / W;
+  if (c0 == c1) return;  // finished inside one CTA
+  float m = -CUDART_INF_F;
+  for (int c = c0 + lane; c <= c1; c += 32) m = fmaxf(m, p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float sum = 0.f;
+  for (int c = c0; c <= c1; ++c) {
+    const int64_t r = static_cast<int64_t>(b) + c;
+    const float w = fast_exp2((p.ws_lse[r * kHq + h] - m) * kLog2e);
+    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + (r * kHq + h) * kHeadDim + 4 * lane);
+    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+    sum += w;
+  }
+  const float inv = 1.0f / sum;
+  *reinterpret_cast<uint2*>(orow) =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = m + logf(sum);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t header, prefix, lse, o, total;
+};
+
+WsLayout ws_layout(int batch, int grid) {
+  WsLayout w;
+  const size_t records = static_cast<size_t>(batch) + grid;
+  w.header = 0;
+  w.prefix = 256;
+  w.lse = align_up(w.prefix + sizeof(int32_t) * (batch + 1), 256);
+  w.o = align_up(w.lse + sizeof(float) * records * kHq, 256);
+  w.total = align_up(w.o + sizeof(float) * records * kHq * kHeadDim, 256);
+  return w;
+}
+
+bool dims_supported(const pa_dims& d) {
+  return d.num_q_heads == kHq && d.num_kv_heads == kHkv && d.head_dim == kHeadDim &&
+         d.page_size == kPage;
+}
+
+}  // namespace
+
+int decode_grid_size() { return sm_count_current_device(); }
+
+}  // namespace pa
+
+extern "C" size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len) {
+  (void)max_seq_len;
+  if (batch < 0) return 0;
+  (void)dims;
+  const int grid = pa::decode_grid_size();
+  if (grid <= 0) return 0;
+  return pa::ws_layout(batch, grid).total;
+}
+
+extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool,
+                                       const void* v_pool, int64_t num_pages,
+                                       const int32_t* block_table, int32_t bt_stride,
+                                       const int32_t* seq_lens, int32_t batch,
+                                       int32_t max_seq_len, float softmax_scale, void* out,
+                                       float* lse, void* workspace, size_t workspace_bytes,
+                                       int32_t* status, pa_stream_t stream) {
+  using namespace pa;
+  if (!dims_supported(dims)) return PA_ERR_UNSUPPORTED;
+  if (batch < 0 || batch > kMaxBatch || bt_stride <= 0 || num_pages <= 0 || max_seq_len < 0 ||
+      max_seq_len > 131072 || !(softmax_scale == softmax_scale))
+    return PA_ERR_INVALID_ARG;
+  if (batch == 0) return PA_OK;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pool) |
+       reinterpret_cast<uintptr_t>(v_pool) | reinterpret_cast<uintptr_t>(out)) & 15u)
+    return PA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
+  const int grid = decode_grid_size();
+  if (grid <= 0) return PA_ERR_CUDA;
+  const WsLayout w = ws_layout(batch, grid);
+  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(DecodeSmem)));
+    if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(decode)");
+    configured_device = dev;
+  }
+
+  DecodeParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_pool = static_cast<const uint8_t*>(k_pool);
+  p.v_pool = static_cast<const uint8_t*>(v_pool);
+  p.num_pages = num_pages;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = seq_lens;
+  p.batch = batch;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_header = reinterpret_cast<int32_t*>(ws + w.header);
+  p.ws_prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
+  p.ws_lse = reinterpret_cast<float*>(ws + w.lse);
+  p.ws_o = reinterpret_cast<float*>(ws + w.o);
+  p.status = status;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  decode_splitkv_kernel<<<grid, kThreads, sizeof(DecodeSmem), st>>>(p);
+  PA_CHECK_LAUNCH("decode_splitkv_kernel");
+  decode_merge_kernel<<<batch, kHq * 32, 0, st>>>(p);
+  PA_CHECK_LAUNCH("decode_merge_kernel");
+  return PA_OK;
+}

@@ -1,0 +1,77 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for sm_103a, loads, and
+exports every function that include/*.h declares; argument errors are rejected before any
+CUDA call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\**([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from long_context_paged_gb300 import build as b
+    b.build()
+    import long_context_paged_gb300 as pa
+    return pa.load()
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("kv_append_paged", "attn_decode_paged", "attn_prefill_chunk", "attn_merge_lse"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert lib.pa_status_string(0) == b"ok"
+    assert lib.pa_status_string(3) == b"workspace too small"
+    assert lib.pa_version() >= 100
+
+
+def test_argument_errors_are_rejected_before_launch(lib):
+    import long_context_paged_gb300 as pa
+    bad_dims = pa.Dims(16, 8, 64, 16)
+    good = pa.Dims(*pa.DEFAULT_DIMS)
+    null = None
+    # unsupported shape
+    assert lib.attn_decode_paged(bad_dims, null, null, null, 1, null, 1, null, 1, 16, 1.0,
+                                 null, null, null, 0, null, null) == 2
+    assert lib.attn_prefill_chunk(pa.Dims(16, 4, 128, 16), null, null, 1, null, null, 1, null, 1,
+                                  null, 1, 1, 16, 1.0, null, null, null, 0, null, null) == 2
+    assert lib.kv_append_paged(pa.Dims(16, 8, 128, 32), null, null, 1, null, null, 1, null, 1,
+                               null, null, 1, null, null) == 2
+    # negative sizes / null pointers
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, -1, 16, 1.0,
+                                 null, null, null, 0, null, null) == 1
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 2, 16, 1.0,
+                                 null, null, null, 0, null, null) == 1
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 1, 200000, 1.0,
+                                 null, null, null, 0, null, null) == 1
+    assert lib.kv_append_paged(good, null, null, -3, null, null, 1, null, 1,
+                               null, null, 1, null, null) == 1
+    assert lib.attn_merge_lse(2, 3, 4, 130, null, null, null, null, null) == 2
+    assert lib.attn_merge_lse(-1, 3, 4, 128, null, null, null, null, null) == 1
+    # empty work is a no-op success
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 0, 16, 1.0,
+                                 null, null, null, 0, null, null) == 0
+    assert lib.attn_merge_lse(1, 0, 16, 128, null, null, null, null, null) == 0
+    assert lib.pa_read_device_status(null, null, null) == 1

@@ -1,0 +1,79 @@
+"""The mixed scheduler step: per layer, append the new tokens, then prefill the chunk and
+decode the other sequences, each layer with its own pools; checked against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import bits, check_attn, host
+
+pytestmark = pytest.mark.gpu
+
+
+def mixed_step(pa, inp, layer, chunk_rows, ws=None):
+    """append + prefill(first sequence) + decode(the rest) for one layer."""
+    B = inp.batch
+    pa.kv_append_paged(inp.k_new[layer], inp.v_new[layer], inp.cu_q_lens, inp.start_pos,
+                       inp.block_table, inp.k_pools[layer], inp.v_pools[layer])
+    q = inp.q[layer]
+    max_s = int(inp.host_seq_lens.max())
+    po, pl = pa.attn_prefill_chunk(q[:chunk_rows], inp.cu_q_lens[:2], inp.k_pools[layer],
+                                   inp.v_pools[layer], inp.block_table[:1], inp.seq_lens[:1],
+                                   chunk_rows, max_s, inp.scale)
+    do, dl = pa.attn_decode_paged(q[chunk_rows:], inp.k_pools[layer], inp.v_pools[layer],
+                                  inp.block_table[1:], inp.seq_lens[1:], max_s, inp.scale,
+                                  workspace=ws)
+    return po, pl, do, dl
+
+
+def oracle_mixed(inp, layer, k_before, v_before, chunk_rows, prefill_rows=None, decode_seqs=None):
+    k, v = oracle.kv_append(bits(inp.k_new[layer]), bits(inp.v_new[layer]), host(inp.cu_q_lens),
+                            host(inp.start_pos), inp.host_block_table, k_before, v_before)
+    q = bits(inp.q[layer])
+    po, pl = oracle.prefill(q[:chunk_rows], [0, chunk_rows], k, v, inp.host_block_table[:1],
+                            inp.host_seq_lens[:1], inp.scale, rows=prefill_rows, threads=16)
+    do, dl = oracle.decode(q[chunk_rows:], k, v, inp.host_block_table[1:],
+                           inp.host_seq_lens[1:], inp.scale, seqs=decode_seqs, threads=16)
+    return po, pl, do, dl
+
+
+def test_mixed_step_reduced(cuda_lib):
+    """Two layers; a 256-query chunk at offset 2,048 plus 7 decodes of 500..9,000 keys."""
+    dec = [500, 9000, 1234, 16, 4097, 7777, 31]
+    inp = W.make_paged(400, [2048 + 256] + dec, [256] + [1] * 7, layers=2, device="cuda")
+    for layer in range(2):
+        kb, vb = bits(inp.k_pools[layer]).copy(), bits(inp.v_pools[layer]).copy()
+        po, pl, do, dl = mixed_step(cuda_lib, inp, layer, 256)
+        torch.cuda.synchronize()
+        ro = oracle_mixed(inp, layer, kb, vb, 256)
+        check_attn(po, pl, ro[0], ro[1], what=f"layer {layer} prefill")
+        check_attn(do, dl, ro[2], ro[3], what=f"layer {layer} decode")
+
+
+def test_mixed_step_full_size_sampled(cuda_lib):
+    """The 28-layer mixed workload at full size (about 173 GB of pools), in the bench's launch
+    configuration; checked on sampled layers, sampled prefill rows and sampled sequences."""
+    free, _ = torch.cuda.mem_get_info()
+    L, ql = W.lengths_for("mixed_28l")
+    need = 28 * 2 * int((-(-L // 16)).sum() + 16) * 32768 + (8 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free, have {free / 2**30:.0f} GiB")
+    inp = W.make_workload("mixed_28l", device="cuda")
+    check_layers = {0, 13, 27}
+    saved = {l: (bits(inp.k_pools[l]).copy(), bits(inp.v_pools[l]).copy()) for l in check_layers}
+    outs = {}
+    for layer in range(28):
+        r = mixed_step(cuda_lib, inp, layer, 4096)
+        if layer in check_layers:
+            outs[layer] = r
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    rows = sorted(set(range(8)) | set(range(4088, 4096)) | set(int(x) for x in rng.integers(0, 4096, 24)))
+    seqs = sorted(set(int(x) for x in rng.integers(0, 31, 6)) | {0, 30})
+    for layer in sorted(check_layers):
+        kb, vb = saved.pop(layer)
+        ro = oracle_mixed(inp, layer, kb, vb, 4096, prefill_rows=rows, decode_seqs=seqs)
+        po, pl, do, dl = outs[layer]
+        check_attn(po, pl, ro[0], ro[1], rows=rows, what=f"layer {layer} prefill")
+        check_attn(do, dl, ro[2], ro[3], rows=seqs, what=f"layer {layer} decode")

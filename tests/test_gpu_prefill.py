@@ -1,0 +1,86 @@
+"""Chunked-prefill parity: the CUDA kernel against the fp64 oracle on the same seeded bytes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import bits, check_attn, host
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(pa, inp, layer=0, status=None):
+    max_q = int(inp.host_q_lens.max())
+    max_s = int(inp.host_seq_lens.max())
+    out, lse = pa.attn_prefill_chunk(inp.q[layer], inp.cu_q_lens, inp.k_pools[layer],
+                                     inp.v_pools[layer], inp.block_table, inp.seq_lens, max_q,
+                                     max_s, inp.scale, status=status)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_prefill(inp, layer=0, rows=None):
+    return oracle.prefill(bits(inp.q[layer]), host(inp.cu_q_lens),
+                          bits(inp.k_pools[layer]), bits(inp.v_pools[layer]),
+                          inp.host_block_table, inp.host_seq_lens, inp.scale, rows=rows,
+                          threads=16)
+
+
+@pytest.mark.parametrize("q_len,offset", [(1, 0), (1, 999), (15, 0), (16, 16), (17, 100),
+                                          (128, 0), (129, 1000), (300, 37), (256, 4096)])
+def test_prefill_single_chunk(cuda_lib, q_len, offset):
+    inp = W.make_paged(100 + q_len, [offset + q_len], [q_len], poison=True, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefill(cuda_lib, inp, status=status)
+    ref_o, ref_l = oracle_prefill(inp)
+    check_attn(out, lse, ref_o, ref_l, what=f"prefill q_len={q_len} offset={offset}")
+    assert cuda_lib.read_device_status(status) == 0
+
+
+def test_prefill_ragged_chunks(cuda_lib):
+    """Several chunks of different lengths and offsets in one call (coalesced prefill)."""
+    q_lens = [7, 128, 1, 200, 64]
+    offsets = [0, 333, 4095, 16, 1000]
+    inp = W.make_paged(200, [o + q for o, q in zip(offsets, q_lens)], q_lens, poison=True,
+                       device="cuda")
+    out, lse = run_prefill(cuda_lib, inp)
+    ref_o, ref_l = oracle_prefill(inp)
+    check_attn(out, lse, ref_o, ref_l, what="ragged chunks")
+
+
+def test_prefill_last_chunk_reduced(cuda_lib):
+    """The last-chunk shape scaled down 8x: 512 queries at offset 7,680, every row checked."""
+    inp = W.make_paged(201, [7680 + 512], [512], poison=True, device="cuda")
+    out, lse = run_prefill(cuda_lib, inp)
+    ref_o, ref_l = oracle_prefill(inp)
+    check_attn(out, lse, ref_o, ref_l, what="512 @ 7680")
+
+
+def sampled_rows(n, seed, count=96):
+    rng = np.random.default_rng(seed)
+    rows = set(range(16)) | set(range(n - 16, n))
+    rows |= {r for r in (15, 16, 17, 127, 128, 129, n // 2) if r < n}
+    rows |= set(int(x) for x in rng.integers(0, n, size=count))
+    return sorted(rows)
+
+
+def test_prefill_full_size_last_chunk(cuda_lib):
+    """4096 queries at offset 61,440 over 65,536 keys, in the bench's launch; sampled rows."""
+    inp = W.make_workload("prefill_4096_at_61440", device="cuda", poison=True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefill(cuda_lib, inp, status=status)
+    rows = sampled_rows(4096, 4)
+    ref_o, ref_l = oracle_prefill(inp, rows=rows)
+    check_attn(out, lse, ref_o, ref_l, rows=rows, what="prefill_4096_at_61440")
+    assert cuda_lib.read_device_status(status) == 0
+
+
+def test_prefill_chunk_longer_than_sequence_is_flagged(cuda_lib):
+    inp = W.make_paged(202, [50], [20], device="cuda")
+    sl = inp.seq_lens.clone()
+    sl[0] = 10
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.attn_prefill_chunk(inp.q[0], inp.cu_q_lens, inp.k_pools[0], inp.v_pools[0],
+                                inp.block_table, sl, 20, 50, inp.scale, status=status)
+    assert cuda_lib.read_device_status(status) & cuda_lib.DEV_ERR_LENGTH
