@@ -124,6 +124,33 @@ pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool, con
                             size_t workspace_bytes, int32_t* status, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * attn_decode_paged_noalloc — attn_decode_paged without a caller-provided workspace.
+ *
+ * The pages have no counterpart of this call; it exists for callers that cannot allocate
+ * device memory: an engine that reserved all free HBM for its own KV-cache pool up front (a
+ * cudaMalloc would fail), a plugin host that exposes no device allocator, or a latency-critical
+ * loop in which cudaMalloc / cudaFree may synchronize the device. The caller still provides q,
+ * the pools, block_table, seq_lens, out and lse exactly as for attn_decode_paged; this call
+ * itself allocates nothing and calls no allocating routine.
+ *
+ * Scratch lives in one fixed 4.5 MiB device array inside the library; every GPU that loads the
+ * library holds it until the process exits. Limit: pa_decode_workspace_size(dims, batch, ...)
+ * must not exceed 4.5 MiB (batch up to about 400 on a 152-SM GB300); larger batches return
+ * PA_ERR_WORKSPACE_TOO_SMALL with the sizes in pa_last_error().
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and caches it; make that first call before any stream capture.
+ * Every call shares the one array and no call needs it zeroed (each call writes every scratch
+ * byte it later reads), so calls that overlap on the GPU (different streams, or several host
+ * threads) race on it and must be serialized by the caller.
+ * ------------------------------------------------------------------------------------------ */
+pa_status attn_decode_paged_noalloc(pa_dims dims, const void* q, const void* k_pool,
+                                    const void* v_pool, int64_t num_pages,
+                                    const int32_t* block_table, int32_t bt_stride,
+                                    const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                    float softmax_scale, void* out, float* lse, int32_t* status,
+                                    pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * attn_prefill_chunk — causal attention of query chunks over their cached prefix + themselves.
  *
  * Source: chunked prefill of long audio prompts in 4096-token pieces ("Optimizing ASR Models

@@ -20,7 +20,8 @@ import torch
 
 __all__ = [
     "load", "PagedAttnError", "Dims", "DEFAULT_DIMS",
-    "kv_append_paged", "attn_decode_paged", "attn_prefill_chunk", "attn_merge_lse",
+    "kv_append_paged", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_prefill_chunk",
+    "attn_merge_lse",
     "decode_workspace_size", "prefill_workspace_size", "read_device_status",
     "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "lib_path",
 ]
@@ -65,6 +66,8 @@ _SIGS = {
     "pa_decode_workspace_size": (_SZ, [Dims, _I32, _I32]),
     "attn_decode_paged": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _P, _P, _P,
                                  _SZ, _P, _P]),
+    "attn_decode_paged_noalloc": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _P,
+                                         _P, _P, _P]),
     "pa_prefill_workspace_size": (_SZ, [Dims, _I32, _I32, _I32]),
     "attn_prefill_chunk": (_I32, [Dims, _P, _P, _I32, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
                                   _F, _P, _P, _P, _SZ, _P, _P]),
@@ -182,6 +185,28 @@ def attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int
         block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), float(softmax_scale),
         _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
+    return out, lse
+
+
+def attn_decode_paged_noalloc(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int,
+                              softmax_scale: float, *, out, lse=None, status=None, stream=None,
+                              dims=None):
+    """attn_decode_paged with the library's fixed scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory: out (and lse, if wanted) must be given;
+    nothing is allocated here or in the library. Calls that overlap on the GPU race on the
+    shared scratch and must be serialized by the caller."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    lib = load()
+    _check("attn_decode_paged_noalloc", lib.attn_decode_paged_noalloc(
+        _dims(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), q.shape[0], int(max_seq_len), float(softmax_scale),
+        _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))
     return out, lse
 
 

@@ -1,5 +1,6 @@
 // Host-side glue of the C ABI: error text, device status word, SM count cache, version.
 #include <cuda_runtime.h>
+#include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -18,6 +19,13 @@ pa_status record_cuda_error(cudaError_t err, const char* where) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(err),
            static_cast<int>(err));
   return PA_ERR_CUDA;
+}
+
+void snprintf_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
 }
 
 int sm_count_current_device() {

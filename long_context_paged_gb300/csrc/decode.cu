@@ -26,6 +26,8 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -524,4 +526,73 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   decode_merge_kernel<<<batch, kHq * 32, 0, st>>>(p);
   PA_CHECK_LAUNCH("decode_merge_kernel");
   return PA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// attn_decode_paged_noalloc: the same decode, with its scratch in a fixed device array.
+//
+// For callers that cannot allocate device memory themselves: an engine that has handed all
+// free HBM to its own KV-cache pool up front (a cudaMalloc would fail), a host process that
+// embeds this library as a plugin without exposing an allocator, or a latency-critical loop
+// where cudaMalloc/cudaFree may synchronize the device. Such a caller still passes q, the
+// pools, the tables and the outputs; the split-KV partials go to g_decode_scratch, a
+// file-scope array that every GPU which loads this library holds until the process exits.
+// ---------------------------------------------------------------------------------------------
+namespace pa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(9) << 19;  // 4.5 MiB
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[64] = {nullptr};
+
+// Device address of g_decode_scratch on the current device. In host code the array's name is
+// only a host-side stand-in, so the address is looked up once per device (with that device
+// current) and cached.
+pa_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda_error(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess) return record_cuda_error(e, "cudaGetSymbolAddress(g_decode_scratch)");
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status attn_decode_paged_noalloc(pa_dims dims, const void* q, const void* k_pool,
+                                               const void* v_pool, int64_t num_pages,
+                                               const int32_t* block_table, int32_t bt_stride,
+                                               const int32_t* seq_lens, int32_t batch,
+                                               int32_t max_seq_len, float softmax_scale,
+                                               void* out, float* lse, int32_t* status,
+                                               pa_stream_t stream) {
+  using namespace pa;
+  if (batch < 0) return PA_ERR_INVALID_ARG;
+  if (batch > 0) {
+    const int grid = decode_grid_size();
+    if (grid <= 0) return PA_ERR_CUDA;
+    const size_t need = ws_layout(batch, grid).total;
+    if (need > kStaticScratchBytes) {
+      snprintf_error("attn_decode_paged_noalloc: batch %d needs %zu bytes of scratch on this GPU, "
+                     "more than the built-in %zu bytes; use attn_decode_paged with a workspace",
+                     batch, need, kStaticScratchBytes);
+      return PA_ERR_WORKSPACE_TOO_SMALL;
+    }
+  }
+  void* scratch = nullptr;
+  const pa_status st = static_scratch(&scratch);
+  if (st != PA_OK) return st;
+  return attn_decode_paged(dims, q, k_pool, v_pool, num_pages, block_table, bt_stride, seq_lens,
+                           batch, max_seq_len, softmax_scale, out, lse, scratch,
+                           kStaticScratchBytes, status, stream);
 }

@@ -21,6 +21,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Host-side error bookkeeping (defined in api.cu).
 // ---------------------------------------------------------------------------------------------
 pa_status record_cuda_error(cudaError_t err, const char* where);
+// printf-style text for pa_last_error() (calling thread).
+void snprintf_error(const char* fmt, ...);
 int sm_count_current_device();
 
 #define PA_CHECK_LAUNCH(where)                                        \
