@@ -205,29 +205,31 @@ class Step:
             self.pf_out = torch.empty(self.n_chunk_rows, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16,
                                       device=device)
             self.pf_lse = torch.empty(self.n_chunk_rows, W.HQ, dtype=torch.float32, device=device)
+            self.pf_ws = torch.empty(max(256, pa.prefill_workspace_size(1, self.n_chunk_rows, self.max_s)),
+                                     dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.launches_per_step = self.layers * ((1 if self.append else 0) + (1 if self.n_chunk_rows else 0)
                                                 + (2 if nd else 0))
 
-    def run(self, events=None, q_src=None):
+    def run(self, events=None, q_src=None, parts=("append", "prefill", "decode")):
         pa, inp = self.pa, self.inp
         stream = torch.cuda.current_stream()
         for layer in range(self.layers):
             q = inp.q[layer] if q_src is None else q_src[layer]
-            if self.append:
+            if self.append and "append" in parts:
                 pa.kv_append_paged(inp.k_new[layer], inp.v_new[layer], inp.cu_q_lens, inp.start_pos,
                                    inp.block_table, inp.k_pools[layer], inp.v_pools[layer],
                                    status=self.status, stream=stream)
-            if self.n_chunk_rows:
+            if self.n_chunk_rows and "prefill" in parts:
                 if events is not None:
                     events["pf"][layer][0].record(stream)
                 pa.attn_prefill_chunk(q[:self.n_chunk_rows], self.pf_cu, inp.k_pools[layer],
                                       inp.v_pools[layer], self.pf_bt, self.pf_sl, self.n_chunk_rows,
                                       self.max_s, inp.scale, out=self.pf_out, lse=self.pf_lse,
-                                      status=self.status, stream=stream)
+                                      workspace=self.pf_ws, status=self.status, stream=stream)
                 if events is not None:
                     events["pf"][layer][1].record(stream)
-            if len(self.dec_idx):
+            if len(self.dec_idx) and "decode" in parts:
                 if events is not None:
                     events["dec"][layer][0].record(stream)
                 pa.attn_decode_paged(q[self.n_chunk_rows:], inp.k_pools[layer], inp.v_pools[layer],
@@ -296,7 +298,8 @@ def e2e_run(step: Step, steps: int):
                 dev_q[:n].copy_(host_q[layer][:n], non_blocking=True)
                 pa.attn_prefill_chunk(dev_q[:n], step.pf_cu, inp.k_pools[layer], inp.v_pools[layer],
                                       step.pf_bt, step.pf_sl, n, step.max_s, inp.scale,
-                                      out=step.pf_out, lse=step.pf_lse, stream=stream)
+                                      out=step.pf_out, lse=step.pf_lse, workspace=step.pf_ws,
+                                      stream=stream)
                 out_pf.copy_(step.pf_out, non_blocking=True)
                 lse_pf.copy_(step.pf_lse, non_blocking=True)
                 ev["pf"][layer][1].record(stream)
@@ -370,6 +373,36 @@ def cpu_baseline(step: Step, budget_s: float = 12.0):
 
 
 # ----------------------------------------------------------------------------------------------
+# CUDA-graph replay: the C-ABI calls are capture-safe (grids from host bounds, no host sync),
+# so each timed phase is captured once and replayed; the device time then has no host gaps.
+# ----------------------------------------------------------------------------------------------
+def capture(step: Step, parts):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step.run(parts=parts)
+    return g
+
+
+def timed_replays(graph, steps, warmup, dist):
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return a.elapsed_time(b) / 1e3
+
+
+# ----------------------------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -400,45 +433,38 @@ def main():
     step = Step(pa, args.workload, dev)
     hbm, bf16, bf16s, peak_src = peaks()
 
-    for _ in range(max(args.warmup, 0)):
-        step.run()
+    step.run()                      # first eager pass: per-device one-time set-up
     torch.cuda.synchronize()
     flags = pa.read_device_status(step.status)
     if flags:
-        raise RuntimeError(f"device status flagged errors during warm-up: {flags}")
+        raise RuntimeError(f"device status flagged errors in the first pass: {flags}")
+    has_dec, has_pf = len(step.dec_idx) > 0, step.n_chunk_rows > 0
+    g_step = capture(step, ("append", "prefill", "decode"))
+    g_dec = capture(step, ("decode",)) if has_dec else None
+    g_pf = capture(step, ("prefill",)) if has_pf and has_dec else None
 
     sampler = ClockSampler(args.clocks_out)
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    all_ev = []
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(args.steps):
-        ev = make_events(step.layers)
-        step.run(events=ev)
-        all_ev.append(ev)
-    stop.record()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
+    W_, K_ = max(args.warmup, 0), args.steps
+    total_s = timed_replays(g_step, K_, W_, dist)
+    t_dec = timed_replays(g_dec, K_, W_, dist) if g_dec is not None else 0.0
+    t_pf = timed_replays(g_pf, K_, W_, dist) if g_pf is not None else 0.0
+    if has_pf and not has_dec:
+        t_pf = total_s
+    if has_dec and not has_pf and not step.append:
+        t_dec = total_s
     clocks = sampler.stop(device_uuid()) if rank == 0 else None
-
-    total_s = start.elapsed_time(stop) / 1e3
-    t_dec = sum(elapsed(e["dec"]) for e in all_ev) if len(step.dec_idx) else 0.0
-    t_pf = sum(elapsed(e["pf"]) for e in all_ev) if step.n_chunk_rows else 0.0
     if dist is not None:
         t = torch.tensor([total_s, t_dec, t_pf], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_s, t_dec, t_pf = t.tolist()
     n = world
-    launches = step.launches_per_step * args.steps
-    dec_gbs = step.dec_bytes * step.layers * args.steps * n / t_dec / 1e9 if t_dec else None
-    pf_tflops = step.pf_flops * step.layers * args.steps * n / t_pf / 1e12 if t_pf else None
+    launches = K_ * (step.launches_per_step + (2 * step.layers if g_dec is not None else 0)
+                     + (step.layers if g_pf is not None else 0))
+    dec_gbs = step.dec_bytes * step.layers * K_ * n / t_dec / 1e9 if t_dec else None
+    pf_tflops = step.pf_flops * step.layers * K_ * n / t_pf / 1e12 if t_pf else None
 
     if pa.read_device_status(step.status):
         raise RuntimeError("device status flagged errors in the timed region")
@@ -462,25 +488,27 @@ def main():
 
     # roofline of the dominant kernel (by device time), the other one alongside
     dec_src = source_hash("decode.cu", "pa_common.cuh")
-    pf_src = source_hash("prefill.cu", "pa_common.cuh")
+    pf_src = source_hash("prefill_tc.cu", "tc_common.cuh", "pa_common.cuh")
     roofs = []
     if t_dec:
-        per_launch_s = t_dec / (step.layers * args.steps)
+        per_launch_s = t_dec / (step.layers * K_)
         ach = step.dec_bytes / per_launch_s / 1e9
         roofs.append((t_dec, {"kernel": "attn_decode_paged (decode_splitkv + merge)", "bound": "hbm",
                               "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(ach / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
-                              "traffic": traffic_from_profile("decode_splitkv_mixed_28l.md", dec_src),
+                              "traffic": traffic_from_profile("decode_splitkv_decode_b16_l27k.md", dec_src)
+                              if args.workload == "mixed_28l" else None,
                               "algorithmic_bytes_per_launch": step.dec_bytes}))
     if t_pf:
-        per_launch_s = t_pf / (step.layers * args.steps)
+        per_launch_s = t_pf / (step.layers * K_)
         ach = step.pf_flops / per_launch_s / 1e12
         pk = bf16s if step.layers > 1 else bf16
         roofs.append((t_pf, {"kernel": "attn_prefill_chunk", "bound": "tensor",
                              "achieved": round(ach, 2), "peak": pk, "unit": "TFLOP/s",
                              "frac": round(ach / pk, 4),
                              "peak_source": f"{peak_src} bf16_tflops" + ("_sustained" if step.layers > 1 else ""),
-                             "traffic": traffic_from_profile("prefill_mixed_28l.md", pf_src),
+                             "traffic": traffic_from_profile("prefill_tc_prefill_4096_at_61440.md", pf_src)
+                             if args.workload == "mixed_28l" else None,
                              "algorithmic_flops_per_launch": step.pf_flops}))
     roofs.sort(key=lambda x: -x[0])
 
@@ -490,7 +518,7 @@ def main():
     line = {
         "metric": "paged GQA attn: decode KV-read GB/s (% HBM peak); prefill-chunk TFLOP/s (% peak)",
         "value": round(value, 2), "unit": unit, "n_gpus": n, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 3),
+        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / K_, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, paged 16, scattered pages)",
         "config": {"workload": args.workload, "layers": step.layers,
@@ -500,7 +528,13 @@ def main():
                    "prefill_offset": int(L[0] - step.n_chunk_rows) if step.n_chunk_rows else None,
                    "heads": "16q/8kv", "head_dim": 128, "page_size": 16,
                    "parallelism": f"replicas x{n}",
-                   "l2": "inputs larger than L2 (each step reads every layer's pools)"},
+                   "l2": "inputs larger than L2 (each step reads every layer's pools)",
+                   "timing": "CUDA events around K CUDA-graph replays each of: the whole step "
+                             "(ms_per_step), its decode calls only (decode GB/s), its prefill "
+                             "calls only (prefill TFLOP/s)"},
+        "phase_ms_per_step": {"step": round(total_s * 1e3 / K_, 3),
+                              "decode": round(t_dec * 1e3 / K_, 3) if t_dec else None,
+                              "prefill": round(t_pf * 1e3 / K_, 3) if t_pf else None},
         "decode": None if dec_gbs is None else {"value": round(dec_gbs, 1), "unit": "GB/s",
                                                  "frac_of_hbm_peak": round(dec_gbs / hbm, 4)},
         "prefill": None if pf_tflops is None else {"value": round(pf_tflops, 2), "unit": "TFLOP/s",

@@ -78,6 +78,39 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return d;
 }
 
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// 2^x of two values on the FMA pipe, leaving the MUFU unit to other elements. x = n + f with
+// n = round(x) taken from the low mantissa bits of x + 1.5*2^23 and f in [-1/2, 1/2]; 2^f is a
+// cubic fitted to 2^f on [-1/2, 1/2] by iteratively reweighted least squares in relative error
+// (max relative error 7.5e-5 in fp32 Horner form, far below the bf16 rounding of P); 2^n is
+// added to the exponent field. Inputs below -126 are clamped (the result is then below 2^-125,
+// i.e. zero for every later use).
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -126.0f);
+  x.y = fmaxf(x.y, -126.0f);
+  const float2 t = add2(x, make_float2(kMagic, kMagic));
+  const float2 r = add2(t, make_float2(-kMagic, -kMagic));
+  const float2 f = add2(x, make_float2(-r.x, -r.y));
+  float2 q = fma2(make_float2(0.0551716685f, 0.0551716685f), f,
+                  make_float2(0.2426111400f, 0.2426111400f));
+  q = fma2(q, f, make_float2(0.6932609677f, 0.6932609677f));
+  q = fma2(q, f, make_float2(0.9999280572f, 0.9999280572f));
+  return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

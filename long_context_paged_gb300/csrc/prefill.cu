@@ -14,14 +14,15 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
                             const void* k_pool, const void* v_pool, int64_t num_pages,
                             const int32_t* block_table, int32_t bt_stride,
                             const int32_t* seq_lens, int32_t batch, int32_t max_q_len,
-                            float softmax_scale, void* out, float* lse, int32_t* status,
-                            cudaStream_t stream);
+                            float softmax_scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, int32_t* status, cudaStream_t stream);
+size_t prefill_workspace_bytes(int batch);
 }  // namespace pa
 
 extern "C" size_t pa_prefill_workspace_size(pa_dims dims, int32_t batch, int32_t max_q_len,
                                             int32_t max_seq_len) {
-  (void)dims; (void)batch; (void)max_q_len; (void)max_seq_len;
-  return 0;
+  (void)dims; (void)max_q_len; (void)max_seq_len;
+  return pa::prefill_workspace_bytes(batch);
 }
 
 extern "C" pa_status attn_prefill_chunk(pa_dims dims, const void* q, const int32_t* cu_q_lens,
@@ -33,13 +34,12 @@ extern "C" pa_status attn_prefill_chunk(pa_dims dims, const void* q, const int32
                                         void* workspace, size_t workspace_bytes,
                                         int32_t* status, pa_stream_t stream) {
   using namespace pa;
-  (void)workspace; (void)workspace_bytes;
   if (dims.num_q_heads != kHq || dims.num_kv_heads != kHkv || dims.head_dim != kHeadDim ||
       dims.page_size != kPage)
     return PA_ERR_UNSUPPORTED;
   if (total_q < 0 || batch < 0 || bt_stride <= 0 || num_pages <= 0 || max_q_len < 0 ||
       max_seq_len < 0 || max_seq_len > 131072 || max_q_len > max_seq_len ||
-      !(softmax_scale > 0.f) || !(softmax_scale < 1e30f) || batch > 65535)
+      !(softmax_scale > 0.f) || !(softmax_scale < 1e30f))
     return PA_ERR_INVALID_ARG;
   if (batch == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
   if (!q || !cu_q_lens || !k_pool || !v_pool || !block_table || !seq_lens || !out)
@@ -48,6 +48,6 @@ extern "C" pa_status attn_prefill_chunk(pa_dims dims, const void* q, const int32
        reinterpret_cast<uintptr_t>(v_pool) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return PA_ERR_INVALID_ARG;
   return launch_prefill_tc(q, total_q, cu_q_lens, k_pool, v_pool, num_pages, block_table,
-                           bt_stride, seq_lens, batch, max_q_len, softmax_scale, out, lse, status,
-                           reinterpret_cast<cudaStream_t>(stream));
+                           bt_stride, seq_lens, batch, max_q_len, softmax_scale, out, lse,
+                           workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
 }

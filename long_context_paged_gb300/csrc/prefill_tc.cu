@@ -6,21 +6,30 @@
 // "MOSS-Transcribe-Diarize" cookbook, "Inference Pipeline"). QK^T and PV are dense
 // contractions here (thousands of queries per KV read), so they run on tcgen05.mma.
 //
-// One CTA = 128 queries of one chunk x both query heads of one KV head (GQA 16/8), i.e. two
-// 128-row M tiles that share every K/V tile read. Per 128-key tile j:
+// Work decomposition. A job is 128 queries of one chunk x both query heads of one KV head
+// (GQA 16/8): two 128-row M tiles that share every K/V tile read. A job's causal key range is
+// J tiles of 128 keys; one (job, key tile) pair is a unit. Units of all jobs are laid end to
+// end (sequence, then KV head, then query tile) and a persistent grid of one CTA per SM takes
+// equal contiguous unit ranges, so the work is balanced to one tile whatever the chunk
+// lengths and offsets. A job cut by range boundaries leaves normalised partial results
+// (o, lse) in the workspace; prefill_merge_kernel combines them by log-sum-exp.
+//
+// Per 128-key tile j of a job:
 //   S_t = Q_t K_j^T         tcgen05.mma, A = Q_t (smem), B = K_j (smem), D = S_t (TMEM fp32)
 //   P_t = softmax part      4 warps per M tile, one thread per row: tcgen05.ld S_t, mask the
-//                           diagonal, exp2, row sum; P_t written back over S_t as bf16
+//                           diagonal, exp2 (3/4 on the MUFU unit, 1/4 by a cubic on the FMA
+//                           pipe), row sum; P_t written back over S_t as bf16
 //   O_t += P_t V_j          tcgen05.mma, A = P_t (TMEM), B = V_j (smem, MN-major), D = O_t
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
-// Warp roles: 0-3 softmax of M tile 0, 4-7 softmax of M tile 1, 8 TMA producer, 9 MMA issuer.
+// Warp roles: 0-3 softmax of M tile 0, 4-7 softmax of M tile 1, 8 TMA producer, 9 MMA issuer,
+// 10-11 idle (they complete the third warpgroup, which gives its registers to the softmax).
 // K/V tiles arrive by tiled TMA straight from the page pools: one 16-token page x 64 dims per
 // copy (a 3-D tensor map over [tokens][kv heads][dims] with 128-byte swizzle), so the block
-// table is applied per page without any gather pass. Pages past the sequence are fetched at an
+// table is applied per page without a gather pass. Pages past the sequence are fetched at an
 // out-of-range coordinate and arrive as zeros; V rows of the last partial page are zeroed in
 // shared memory before use, so unwritten slots can never reach P*V.
-// The running row max is moved only when a tile exceeds it by more than 8 (log2 units); O is
-// then rescaled in TMEM by its owning warps, after the previous P*V has completed.
+// The running row max moves only when a tile exceeds it by more than 8 (log2 units); O is then
+// rescaled in TMEM by its owning warps, after the previous P*V has completed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -35,25 +44,38 @@
 namespace pa {
 namespace {
 
-constexpr int kTileM = 128;   // queries per CTA (per head)
+constexpr int kTileM = 128;   // queries per job (per head)
 constexpr int kTileN = 128;   // keys per K/V tile
-constexpr int kThreads = 320; // 8 softmax warps + producer + MMA
+constexpr int kThreads = 384; // 8 softmax warps + producer + MMA + 2 spare (3 warpgroups)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kBlockBytes = 128 * 128;  // 128 rows x 64 bf16 (one swizzled 64-dim block)
 constexpr uint32_t kTileBytes = 2 * kBlockBytes;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kMaxBatch = 1024;
+// Register split: the two softmax warpgroups grow to 216 registers per thread, the
+// producer/MMA warpgroup shrinks to 72; 256 * 216 + 128 * 72 = 64,512 = 384 threads x 168, the
+// budget the CTA is launched with (checked on the host before every launch).
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 72;
+constexpr int kLaunchRegs = (256 * kSoftmaxRegs + 128 * kControlRegs) / kThreads;
+// A partial result: o [2 heads][128 rows][128] fp32, then lse [2][128] fp32.
+constexpr size_t kRecordO = 2 * 128 * 128 * sizeof(float);
+constexpr size_t kRecordBytes = kRecordO + 2 * 128 * sizeof(float);
 
 struct __align__(1024) PrefillTcSmem {
   uint8_t q[2][2][kBlockBytes];   // [M tile][64-dim block]
   uint8_t k[2][2][kBlockBytes];   // [stage][64-dim block]
   uint8_t v[2][2][kBlockBytes];
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2], o_ready[2];
+  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
+  long long warp_sums[kThreads / 32];
+  long long total_units;
+  long long unit_prefix[kMaxBatch + 1];  // first unit of each sequence
 };
 
 struct PrefillTcParams {
@@ -61,17 +83,165 @@ struct PrefillTcParams {
   const int32_t* seq_lens;
   const int32_t* block_table;
   int32_t bt_stride;
+  int32_t batch;
   int64_t num_pages;
   float scale_log2;
   uint16_t* out;
   float* lse;
   int32_t* status;
+  long long* ws_header;   // [0] units per CTA, [1] total units
+  long long* ws_prefix;   // [batch + 1]
+  uint8_t* ws_records;    // [2 * grid][kRecordBytes]
+};
+
+// ---------------------------------------------------------------------------------------------
+// Job geometry of one sequence (same arithmetic in every role and in the merge kernel).
+// ---------------------------------------------------------------------------------------------
+struct SeqGeom {
+  int q0, n, L, off, nqt;
+  long long a, Jlast, T;  // full-tile J is a + qt; the last tile's is Jlast; T = units per head
+};
+
+__device__ __forceinline__ SeqGeom seq_geom(const PrefillTcParams& p, int b, bool report) {
+  SeqGeom s;
+  s.q0 = p.cu_q_lens[b];
+  s.n = p.cu_q_lens[b + 1] - s.q0;
+  s.L = p.seq_lens[b];
+  s.nqt = 0;
+  s.off = s.L - s.n;
+  s.a = s.Jlast = s.T = 0;
+  if (s.n <= 0) return s;
+  if (s.n > s.L || s.L > p.bt_stride * kPage) {
+    if (report) flag_error(p.status, PA_DEV_ERR_LENGTH);
+    return s;
+  }
+  s.nqt = (s.n + kTileM - 1) / kTileM;
+  s.a = (s.off + kTileN - 1) / kTileN + 1;
+  s.Jlast = (s.off + s.n - 1) / kTileN + 1;
+  const long long full = s.nqt - 1;
+  s.T = full * s.a + full * (full - 1) / 2 + s.Jlast;
+  return s;
+}
+
+__device__ __forceinline__ long long tiles_of(const SeqGeom& s, int qt) {
+  return qt < s.nqt - 1 ? s.a + qt : s.Jlast;
+}
+__device__ __forceinline__ long long units_before(const SeqGeom& s, int qt) {
+  return static_cast<long long>(qt) * s.a + static_cast<long long>(qt) * (qt - 1) / 2;
+}
+
+// One job piece this CTA owns: key tiles [jb, je) of job (b, g, qt).
+struct Piece {
+  int b, g, qt;
+  SeqGeom s;
+  long long u0;  // first unit of the job
+  int J, jb, je;
+  bool valid;
+};
+
+struct JobWalker {
+  const PrefillTcParams* p;
+  const long long* prefix;
+  long long U0, U1;
+  Piece cur;
+
+  __device__ void set(int b, int g, int qt, long long u0, const SeqGeom& s) {
+    cur.b = b;
+    cur.g = g;
+    cur.qt = qt;
+    cur.s = s;
+    cur.u0 = u0;
+    cur.J = static_cast<int>(tiles_of(s, qt));
+    cur.jb = static_cast<int>(max(U0, u0) - u0);
+    cur.je = static_cast<int>(min(U1, u0 + cur.J) - u0);
+    cur.valid = u0 < U1 && cur.jb < cur.je;
+  }
+
+  __device__ void start(const PrefillTcParams& pp, const long long* pre, long long u_begin,
+                        long long u_end) {
+    p = &pp;
+    prefix = pre;
+    U0 = u_begin;
+    U1 = u_end;
+    int lo = 0, hi = pp.batch;  // last b with prefix[b] <= U0 < prefix[b+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= U0) lo = mid; else hi = mid;
+    }
+    const SeqGeom s = seq_geom(pp, lo, false);
+    const long long rem = U0 - pre[lo];
+    const int g = static_cast<int>(rem / s.T);
+    const long long rem2 = rem - g * s.T;
+    int qt = 0;
+    while (qt + 1 < s.nqt && units_before(s, qt + 1) <= rem2) ++qt;
+    set(lo, g, qt, pre[lo] + g * s.T + units_before(s, qt), s);
+  }
+
+  __device__ void next() {
+    long long u0 = cur.u0 + cur.J;
+    int b = cur.b, g = cur.g, qt = cur.qt + 1;
+    SeqGeom s = cur.s;
+    if (qt >= s.nqt) {
+      qt = 0;
+      if (++g >= kHkv) {
+        g = 0;
+        do {
+          ++b;
+          if (b >= p->batch) {
+            cur.valid = false;
+            return;
+          }
+          s = seq_geom(*p, b, false);
+        } while (s.nqt == 0);
+        u0 = prefix[b];
+      }
+    }
+    set(b, g, qt, u0, s);
+  }
 };
 
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int32_t* status) {
   if (mbar_wait_bounded(bar, parity)) return true;
   flag_error(status, PA_DEV_ERR_TIMEOUT);
   return false;
+}
+
+__device__ __forceinline__ long long warp_incl_scan64(long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// unit_prefix[b] = first unit of sequence b (8 heads x T_b units each).
+__device__ void build_unit_prefix(const PrefillTcParams& p, PrefillTcSmem& s) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (p.batch + kThreads - 1) / kThreads;
+  const int b0 = min(p.batch, tid * per), b1 = min(p.batch, b0 + per);
+  long long local = 0;
+  for (int b = b0; b < b1; ++b) local += kHkv * seq_geom(p, b, blockIdx.x == 0).T;
+  const long long incl = warp_incl_scan64(local, lane);
+  if (lane == 31) s.warp_sums[warp] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    long long run = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const long long v = s.warp_sums[w];
+      s.warp_sums[w] = run;
+      run += v;
+    }
+    s.total_units = run;
+  }
+  __syncthreads();
+  long long run = s.warp_sums[warp] + incl - local;
+  for (int b = b0; b < b1; ++b) {
+    s.unit_prefix[b] = run;
+    run += kHkv * seq_geom(p, b, false).T;
+  }
+  if (tid == 0) s.unit_prefix[p.batch] = s.total_units;
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -81,24 +251,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   PrefillTcSmem& s = *reinterpret_cast<PrefillTcSmem*>(base);
-
-  const int b = blockIdx.z, g = blockIdx.y, qt = blockIdx.x;
-  const int q0 = p.cu_q_lens[b];
-  const int n = p.cu_q_lens[b + 1] - q0;
-  const int row0 = qt * kTileM;
-  if (n <= 0 || row0 >= n) return;
-  const int L = p.seq_lens[b];
-  if (n > L || L > p.bt_stride * kPage) {
-    if (threadIdx.x == 0 && qt == 0 && g == 0) flag_error(p.status, PA_DEV_ERR_LENGTH);
-    return;
-  }
-  const int off = L - n;                                  // position of the chunk's first query
-  const int last_key = off + min(n, row0 + kTileM) - 1;   // largest key any row here sees
-  const int J = last_key / kTileN + 1;                    // K/V tiles to visit
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  build_unit_prefix(p, s);
+  const long long total = s.total_units;
+  const long long W = (total + gridDim.x - 1) / gridDim.x;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) {
+      p.ws_header[0] = W;
+      p.ws_header[1] = total;
+    }
+    for (int b = threadIdx.x; b <= p.batch; b += kThreads) p.ws_prefix[b] = s.unit_prefix[b];
+  }
+  const long long U0 = blockIdx.x * W, U1 = min(total, U0 + W);
+  if (U0 >= U1) return;  // uniform across the CTA: nothing allocated yet
+
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
+    mbar_init(&s.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
@@ -107,6 +277,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 128);
       mbar_init(&s.o_ready[i], 1);
+      mbar_init(&s.o_free[i], 128);
     }
     mbar_init(&s.mma_done, 1);
     fence_mbar_init();
@@ -117,62 +288,85 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
 
+  JobWalker jw;
+  jw.start(p, s.unit_prefix, U0, U1);
+
+  if (warp >= 8) {
+    tc::regs_decrease<kControlRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
     const int oob_token = static_cast<int>(p.num_pages * kPage);  // zero-filled coordinate
-    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-    auto page_token = [&](int j) {
-      int tok = oob_token;
-      const int key0 = j * kTileN + kPage * lane;
-      if (lane < kTileN / kPage && key0 < L) {
-        const int e = bt_row[key0 / kPage];
-        if (e < 0 || e >= p.num_pages) {
-          flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
-          tok = 0;
-        } else {
-          tok = e * kPage;
-        }
-      }
-      return tok;
-    };
     bool ok = true;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&s.q_full, 4 * kBlockBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int kb = 0; kb < 2; ++kb)
-          tc::tma_load_3d(s.q[t][kb], &q_map, kb * 64, 2 * g + t, q0 + row0, &s.q_full);
-    }
-    int tok = page_token(0);
-    for (int j = 0; j < J && ok; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      const int tok_next = (j + 1 < J) ? page_token(j + 1) : 0;
-      if (lane == 0) ok = wait_or_flag(&s.k_empty[st], ph ^ 1u, p.status);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
-#pragma unroll
-      for (int pg = 0; pg < kTileN / kPage; ++pg) {
-        const int t = __shfl_sync(0xffffffffu, tok, pg);
-        if (lane == 0) {
-          tc::tma_load_3d(s.k[st][0] + pg * 2048, &k_map, 0, g, t, &s.k_full[st]);
-          tc::tma_load_3d(s.k[st][1] + pg * 2048, &k_map, 64, g, t, &s.k_full[st]);
+    uint32_t it = 0, jc = 0;
+    for (; jw.cur.valid && ok; jw.next()) {
+      const Piece& pc = jw.cur;
+      const int32_t* bt_row = p.block_table + static_cast<int64_t>(pc.b) * p.bt_stride;
+      auto page_token = [&](int j) {
+        int tok = oob_token;
+        const int key0 = j * kTileN + kPage * lane;
+        if (lane < kTileN / kPage && key0 < pc.s.L) {
+          const int e = bt_row[key0 / kPage];
+          if (e < 0 || e >= p.num_pages) {
+            flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
+            tok = 0;
+          } else {
+            tok = e * kPage;
+          }
+        }
+        return tok;
+      };
+      int tok = page_token(pc.jb);
+      if (lane == 0) {
+        ok = wait_or_flag(&s.q_empty, (jc & 1) ^ 1u, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(&s.q_full, 4 * kBlockBytes);
+          for (int t = 0; t < 2; ++t)
+            for (int kb = 0; kb < 2; ++kb)
+              tc::tma_load_3d(s.q[t][kb], &q_map, kb * 64, 2 * pc.g + t,
+                              pc.s.q0 + pc.qt * kTileM, &s.q_full);
         }
       }
-      if (lane == 0) ok = wait_or_flag(&s.v_empty[st], ph ^ 1u, p.status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
+      for (int j = pc.jb; j < pc.je && ok; ++j, ++it) {
+        const int st = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        const int tok_next = (j + 1 < pc.je) ? page_token(j + 1) : 0;
+        if (lane == 0) ok = wait_or_flag(&s.k_empty[st], ph ^ 1u, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
 #pragma unroll
-      for (int pg = 0; pg < kTileN / kPage; ++pg) {
-        const int t = __shfl_sync(0xffffffffu, tok, pg);
-        if (lane == 0) {
-          tc::tma_load_3d(s.v[st][0] + pg * 2048, &v_map, 0, g, t, &s.v_full[st]);
-          tc::tma_load_3d(s.v[st][1] + pg * 2048, &v_map, 64, g, t, &s.v_full[st]);
+        for (int pg = 0; pg < kTileN / kPage; ++pg) {
+          const int t = __shfl_sync(0xffffffffu, tok, pg);
+          if (lane == 0) {
+            tc::tma_load_3d(s.k[st][0] + pg * 2048, &k_map, 0, pc.g, t, &s.k_full[st]);
+            tc::tma_load_3d(s.k[st][1] + pg * 2048, &k_map, 64, pc.g, t, &s.k_full[st]);
+          }
         }
+        if (lane == 0) ok = wait_or_flag(&s.v_empty[st], ph ^ 1u, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
+#pragma unroll
+        for (int pg = 0; pg < kTileN / kPage; ++pg) {
+          const int t = __shfl_sync(0xffffffffu, tok, pg);
+          if (lane == 0) {
+            tc::tma_load_3d(s.v[st][0] + pg * 2048, &v_map, 0, pc.g, t, &s.v_full[st]);
+            tc::tma_load_3d(s.v[st][1] + pg * 2048, &v_map, 64, pc.g, t, &s.v_full[st]);
+          }
+        }
+        tok = tok_next;
       }
-      tok = tok_next;
+      ++jc;
     }
+    // do not leave while copies into this CTA's shared memory may still be landing
+    if (lane == 0 && it > 0) {
+      for (uint32_t k = (it >= 2 ? it - 2 : 0); k < it; ++k) {
+        wait_or_flag(&s.k_full[k & 1], (k >> 1) & 1, p.status);
+        wait_or_flag(&s.v_full[k & 1], (k >> 1) & 1, p.status);
+      }
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t id_s = tc::idesc_bf16(128, kTileN, 0, 0);    // S = Q K^T
@@ -196,66 +390,79 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       }
     };
     bool ok = true;
-    if (lane == 0) {
-      ok = wait_or_flag(&s.q_full, 0, p.status) && wait_or_flag(&s.k_full[0], 0, p.status);
-      if (ok) {
-        tc::fence_after_sync();
-        issue_s(0, 0);
-        tc::mma_commit(&s.s_full[0]);
-        issue_s(1, 0);
-        tc::mma_commit(&s.s_full[1]);
-        tc::mma_commit(&s.k_empty[0]);
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    for (int j = 0; j < J && ok; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (lane == 0) ok = wait_or_flag(&s.v_full[st], ph, p.status);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const int first_bad = L - j * kTileN;  // V rows at or past this row are not keys
-      if (first_bad < kTileN) {
-        // zero them so that P = 0 there cannot meet an unwritten (possibly NaN) slot
-        const int r0 = max(first_bad, 0);
-        for (int e = r0 * 16 + lane; e < kTileN * 16; e += 32) {
-          const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
-          *reinterpret_cast<uint4*>(s.v[st][c >> 3] + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-      }
+    uint32_t it = 0, jc = 0;
+    for (; jw.cur.valid && ok; jw.next()) {
+      const Piece& pc = jw.cur;
+      const int nt = pc.je - pc.jb;
       if (lane == 0) {
-        ok = wait_or_flag(&s.p_full[0], j & 1, p.status);
+        const int st = it & 1;
+        ok = wait_or_flag(&s.q_full, jc & 1, p.status) &&
+             wait_or_flag(&s.k_full[st], (it >> 1) & 1, p.status);
         if (ok) {
           tc::fence_after_sync();
-          issue_pv(0, st, j > 0);
-          tc::mma_commit(&s.o_ready[0]);
-          if (j + 1 < J) {
-            const int st1 = (j + 1) & 1;
-            ok = wait_or_flag(&s.k_full[st1], ((j + 1) >> 1) & 1, p.status);
-            if (ok) {
-              tc::fence_after_sync();
-              issue_s(0, st1);
-              tc::mma_commit(&s.s_full[0]);
+          issue_s(0, st);
+          tc::mma_commit(&s.s_full[0]);
+          issue_s(1, st);
+          tc::mma_commit(&s.s_full[1]);
+          tc::mma_commit(&s.k_empty[st]);
+          if (nt == 1) tc::mma_commit(&s.q_empty);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      for (int i = 0; i < nt && ok; ++i) {
+        const uint32_t cur = it + i;
+        const int st = cur & 1;
+        if (lane == 0) ok = wait_or_flag(&s.v_full[st], (cur >> 1) & 1, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int first_bad = pc.s.L - (pc.jb + i) * kTileN;  // V rows from here are not keys
+        if (first_bad < kTileN) {
+          // zero them so that P = 0 there cannot meet an unwritten (possibly NaN) slot
+          const int r0 = max(first_bad, 0);
+          for (int e = r0 * 16 + lane; e < kTileN * 16; e += 32) {
+            const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
+            *reinterpret_cast<uint4*>(s.v[st][c >> 3] + r * 128 + (c & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const int st1 = (cur + 1) & 1;
+          ok = wait_or_flag(&s.p_full[0], cur & 1, p.status);
+          if (ok && i == 0 && jc > 0) ok = wait_or_flag(&s.o_free[0], (jc - 1) & 1, p.status);
+          if (ok) {
+            tc::fence_after_sync();
+            issue_pv(0, st, i > 0);
+            tc::mma_commit(&s.o_ready[0]);
+            if (i + 1 < nt) {
+              ok = wait_or_flag(&s.k_full[st1], ((cur + 1) >> 1) & 1, p.status);
+              if (ok) {
+                tc::fence_after_sync();
+                issue_s(0, st1);
+                tc::mma_commit(&s.s_full[0]);
+              }
+            }
+          }
+          if (ok) ok = wait_or_flag(&s.p_full[1], cur & 1, p.status);
+          if (ok && i == 0 && jc > 0) ok = wait_or_flag(&s.o_free[1], (jc - 1) & 1, p.status);
+          if (ok) {
+            tc::fence_after_sync();
+            issue_pv(1, st, i > 0);
+            tc::mma_commit(&s.o_ready[1]);
+            tc::mma_commit(&s.v_empty[st]);
+            if (i + 1 < nt) {
+              issue_s(1, st1);
+              tc::mma_commit(&s.s_full[1]);
+              tc::mma_commit(&s.k_empty[st1]);
+              if (i + 2 == nt) tc::mma_commit(&s.q_empty);
             }
           }
         }
-        if (ok) ok = wait_or_flag(&s.p_full[1], j & 1, p.status);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_pv(1, st, j > 0);
-          tc::mma_commit(&s.o_ready[1]);
-          tc::mma_commit(&s.v_empty[st]);
-          if (j + 1 < J) {
-            const int st1 = (j + 1) & 1;
-            issue_s(1, st1);
-            tc::mma_commit(&s.s_full[1]);
-            tc::mma_commit(&s.k_empty[st1]);
-          }
-        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      it += nt;
+      ++jc;
     }
     // every MMA this thread issued must have finished before TMEM is released
     if (lane == 0) {
@@ -263,108 +470,153 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       wait_or_flag(&s.mma_done, 0, p.status);
     }
     __syncwarp();
+  }
   } else {
+    tc::regs_increase<kSoftmaxRegs>();
     // ------------------------------------------------------------------ softmax warps
     const int t = warp >> 2;                       // M tile = query head 2g + t
     const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;             // row of the tile
-    const int qrow = row0 + r;
-    const int qpos = off + qrow;                   // absolute position of this query
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_bits + t * 128;
     const uint32_t t_o = tmem + lane_bits + 256 + t * 128;
-    float m_used = -CUDART_INF_F, l = 0.f;
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
     bool ok = true;
-    for (int j = 0; j < J; ++j) {
-      ok = __all_sync(0xffffffffu, wait_or_flag(&s.s_full[t], j & 1, p.status));
+    uint32_t it = 0;
+    for (; jw.cur.valid && ok; jw.next()) {
+      const Piece& pc = jw.cur;
+      const int nt = pc.je - pc.jb;
+      const int qrow = pc.qt * kTileM + r;
+      const int qpos = pc.s.off + qrow;            // absolute position of this query
+      float m_used = -CUDART_INF_F, l = 0.f;
+      for (int i = 0; i < nt; ++i) {
+        const uint32_t cur = it + i;
+        ok = __all_sync(0xffffffffu, wait_or_flag(&s.s_full[t], cur & 1, p.status));
+        if (!ok) break;
+        tc::fence_after_sync();
+        uint32_t sb[128];  // raw scores (fp32 bits) of this row
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sb + c * 32));
+        tc::tmem_wait_ld();
+        const int k0 = (pc.jb + i) * kTileN;
+        if (k0 + kTileN - 1 > qpos) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (k0 + c > qpos) sb[c] = 0xff800000u;  // -inf: key after this query
+        }
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sb[c]));
+        const float mx2 = mx * p.scale_log2;
+        const bool grow = mx2 > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? mx2 : m_used;
+          const float alpha = (m_used == -CUDART_INF_F) ? 0.f : fast_exp2(m_used - m_new);
+          if (i > 0) {
+            // O_t holds the sum through the previous tile once its P*V has completed
+            ok = __all_sync(0xffffffffu, wait_or_flag(&s.o_ready[t], (cur - 1) & 1, p.status));
+            if (!ok) break;
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o32[32];
+              tc::tmem_ld32(t_o + c * 32, o32);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o32[k] = __float_as_uint(__uint_as_float(o32[k]) * alpha);
+              tc::tmem_st32(t_o + c * 32, o32);
+            }
+            tc::tmem_wait_st();
+          }
+          l *= alpha;
+          m_used = m_new;
+        }
+        // probabilities (bf16) over S's first 64 columns. A row that has not met a visible key
+        // yet (its piece starts past the row's position) keeps m_used = -inf; a finite offset
+        // then gives exp2(-inf) = 0 for its masked scores instead of NaN.
+        const float m_eff = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+        const float2 nm2 = make_float2(-m_eff, -m_eff);
+        float2 lsum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float2 x = fma2(make_float2(__uint_as_float(sb[c * 64 + 2 * k]),
+                                              __uint_as_float(sb[c * 64 + 2 * k + 1])), sc2, nm2);
+            float2 e;
+            if ((k & 3) == 3) {
+              e = exp2_poly2(x);
+            } else {
+              e.x = fast_exp2(x.x);
+              e.y = fast_exp2(x.y);
+            }
+            lsum = add2(lsum, e);
+            pk[k] = pack_bf16x2(e.x, e.y);
+          }
+          tc::tmem_st32(t_s + c * 32, pk);
+        }
+        l += lsum.x + lsum.y;
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        mbar_arrive(&s.p_full[t]);
+      }
+      if (!ok) break;
+      // epilogue of the piece: O / l
+      ok = __all_sync(0xffffffffu, wait_or_flag(&s.o_ready[t], (it + nt - 1) & 1, p.status));
       if (!ok) break;
       tc::fence_after_sync();
-      float sv[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tc::tmem_ld32(t_s + c * 32, rr);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(rr[i]);
-      }
-      const int k0 = j * kTileN;
-      if (k0 + kTileN - 1 > qpos) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (k0 + c > qpos) sv[c] = -CUDART_INF_F;
-      }
-      float mx = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, sv[c]);
-      const float mx2 = mx * p.scale_log2;
-      const bool grow = mx2 > m_used + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? mx2 : m_used;
-        const float alpha = (m_used == -CUDART_INF_F) ? 0.f : fast_exp2(m_used - m_new);
-        if (j > 0) {
-          // O_t holds the sum through tile j-1 once the previous P*V has completed
-          ok = __all_sync(0xffffffffu, wait_or_flag(&s.o_ready[t], (j - 1) & 1, p.status));
-          if (!ok) break;
-          tc::fence_after_sync();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t rr[32];
-            tc::tmem_ld32(t_o + c * 32, rr);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tc::tmem_st32(t_o + c * 32, rr);
-          }
-          tc::tmem_wait_st();
-        }
-        l *= alpha;
-        m_used = m_new;
-      }
-      // probabilities (bf16) over S's first 64 columns
-      const float neg_m = -m_used;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = fast_exp2(fmaf(sv[c * 64 + 2 * i], p.scale_log2, neg_m));
-          const float p1 = fast_exp2(fmaf(sv[c * 64 + 2 * i + 1], p.scale_log2, neg_m));
-          l += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tc::tmem_st32(t_s + c * 32, pk);
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      mbar_arrive(&s.p_full[t]);
-    }
-    // epilogue: O / l -> bf16 rows, LSE
-    if (ok) ok = __all_sync(0xffffffffu, wait_or_flag(&s.o_ready[t], (J - 1) & 1, p.status));
-    if (ok) {
-      tc::fence_after_sync();
-      const bool live = qrow < n;
+      const bool live = qrow < pc.s.n;
       const float inv = 1.0f / l;
-      uint16_t* dst = p.out + (static_cast<int64_t>(q0 + qrow) * kHq + 2 * g + t) * kHeadDim;
+      const bool whole = pc.jb == 0 && pc.je == pc.J;
+      const int head = 2 * pc.g + t;
+      if (whole) {
+        uint16_t* dst = p.out + (static_cast<int64_t>(pc.s.q0 + qrow) * kHq + head) * kHeadDim;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tc::tmem_ld32(t_o + c * 32, rr);
-        tc::tmem_wait_ld();
-        if (live) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o32[32];
+          tc::tmem_ld32(t_o + c * 32, o32);
+          tc::tmem_wait_ld();
+          if (live) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(rr[8 * i + 0]) * inv, __uint_as_float(rr[8 * i + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(rr[8 * i + 2]) * inv, __uint_as_float(rr[8 * i + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(rr[8 * i + 4]) * inv, __uint_as_float(rr[8 * i + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(rr[8 * i + 6]) * inv, __uint_as_float(rr[8 * i + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + 8 * i) = w;
+            for (int k = 0; k < 4; ++k) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o32[8 * k + 0]) * inv, __uint_as_float(o32[8 * k + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o32[8 * k + 2]) * inv, __uint_as_float(o32[8 * k + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o32[8 * k + 4]) * inv, __uint_as_float(o32[8 * k + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o32[8 * k + 6]) * inv, __uint_as_float(o32[8 * k + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c * 32 + 8 * k) = w;
+            }
           }
         }
+        if (live && p.lse != nullptr)
+          p.lse[static_cast<int64_t>(pc.s.q0 + qrow) * kHq + head] = (m_used + log2f(l)) * kLn2;
+      } else {
+        // a piece of a job shared with neighbouring CTAs: slot 1 if it starts the job, else 0.
+        // A row that saw no key in this piece contributes nothing: o = 0, lse = -inf.
+        const int slot = pc.jb == 0 ? 1 : 0;
+        const bool empty = m_used == -CUDART_INF_F;
+        const float sc_o = empty ? 0.f : inv;
+        uint8_t* rec = p.ws_records + (2 * static_cast<size_t>(blockIdx.x) + slot) * kRecordBytes;
+        float* dst = reinterpret_cast<float*>(rec) + (t * 128 + r) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o32[32];
+          tc::tmem_ld32(t_o + c * 32, o32);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            reinterpret_cast<float4*>(dst + c * 32)[k] =
+                make_float4(__uint_as_float(o32[4 * k]) * sc_o, __uint_as_float(o32[4 * k + 1]) * sc_o,
+                            __uint_as_float(o32[4 * k + 2]) * sc_o, __uint_as_float(o32[4 * k + 3]) * sc_o);
+        }
+        reinterpret_cast<float*>(rec + kRecordO)[t * 128 + r] =
+            empty ? -CUDART_INF_F : (m_used + log2f(l)) * kLn2;
       }
-      if (live && p.lse != nullptr)
-        p.lse[static_cast<int64_t>(q0 + qrow) * kHq + 2 * g + t] = (m_used + log2f(l)) * kLn2;
+      tc::fence_before_sync();
+      mbar_arrive(&s.o_free[t]);
+      it += nt;
     }
   }
 
@@ -376,8 +628,63 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   }
 }
 
+// Combine the pieces of jobs that were cut by CTA range boundaries. One CTA per job; thread =
+// (head, row). The pieces are slot 1 of the first CTA and slot 0 of each later CTA.
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParams p) {
+  const int b = blockIdx.z, g = blockIdx.y, qt = blockIdx.x;
+  const SeqGeom s = seq_geom(p, b, false);
+  if (qt >= s.nqt) return;
+  const long long W = p.ws_header[0];
+  const long long u0 = p.ws_prefix[b] + g * s.T + units_before(s, qt);
+  const long long J = tiles_of(s, qt);
+  const long long c0 = u0 / W, c1 = (u0 + J - 1) / W;
+  if (c0 == c1) return;
+  const int t = threadIdx.x >> 7, r = threadIdx.x & 127;
+  const int qrow = qt * kTileM + r;
+  if (qrow >= s.n) return;
+  auto rec_of = [&](long long c) {
+    return p.ws_records + (2 * static_cast<size_t>(c) + (c == c0 ? 1 : 0)) * kRecordBytes;
+  };
+  float m = -CUDART_INF_F;
+  for (long long c = c0; c <= c1; ++c)
+    m = fmaxf(m, reinterpret_cast<const float*>(rec_of(c) + kRecordO)[t * 128 + r]);
+  float acc[kHeadDim];
+#pragma unroll
+  for (int d = 0; d < kHeadDim; ++d) acc[d] = 0.f;
+  float sum = 0.f;
+  for (long long c = c0; c <= c1; ++c) {
+    const uint8_t* rec = rec_of(c);
+    const float lp = reinterpret_cast<const float*>(rec + kRecordO)[t * 128 + r];
+    if (lp == -CUDART_INF_F) continue;  // the piece held no key visible to this row
+    const float w = fast_exp2((lp - m) * kLog2e);
+    sum += w;
+    const float4* o = reinterpret_cast<const float4*>(rec) + (t * 128 + r) * (kHeadDim / 4);
+#pragma unroll
+    for (int d = 0; d < kHeadDim / 4; ++d) {
+      const float4 v = o[d];
+      acc[4 * d] += w * v.x;
+      acc[4 * d + 1] += w * v.y;
+      acc[4 * d + 2] += w * v.z;
+      acc[4 * d + 3] += w * v.w;
+    }
+  }
+  const float inv = 1.0f / sum;
+  const int head = 2 * g + t;
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(s.q0 + qrow) * kHq + head) * kHeadDim);
+#pragma unroll
+  for (int k = 0; k < kHeadDim / 8; ++k) {
+    uint4 w;
+    w.x = pack_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
+    w.y = pack_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
+    w.z = pack_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
+    w.w = pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+    dst[k] = w;
+  }
+  if (p.lse != nullptr) p.lse[static_cast<int64_t>(s.q0 + qrow) * kHq + head] = m + logf(sum);
+}
+
 // ---------------------------------------------------------------------------------------------
-// host side: tensor maps (driver entry point looked up once), launch
+// host side: tensor maps (driver entry point looked up once), workspace layout, launch
 // ---------------------------------------------------------------------------------------------
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -408,15 +715,45 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t outer, uint64_t heads
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct PrefillWs {
+  size_t header, prefix, records, total;
+};
+
+PrefillWs prefill_ws(int batch, int grid) {
+  PrefillWs w;
+  w.header = 0;
+  w.prefix = 256;
+  w.records = align256(w.prefix + sizeof(long long) * (batch + 1));
+  w.total = align256(w.records + 2 * static_cast<size_t>(grid) * kRecordBytes);
+  return w;
+}
+
 }  // namespace
+
+size_t prefill_workspace_bytes(int batch) {
+  const int grid = sm_count_current_device();
+  if (grid <= 0 || batch < 0) return 0;
+  return prefill_ws(batch, grid).total;
+}
 
 pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_lens,
                             const void* k_pool, const void* v_pool, int64_t num_pages,
                             const int32_t* block_table, int32_t bt_stride,
                             const int32_t* seq_lens, int32_t batch, int32_t max_q_len,
-                            float softmax_scale, void* out, float* lse, int32_t* status,
-                            cudaStream_t stream) {
-  if (num_pages * kPage >= (int64_t(1) << 31) || total_q >= (1 << 30)) return PA_ERR_UNSUPPORTED;
+                            float softmax_scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
+  if (batch > kMaxBatch) {
+    snprintf_error("attn_prefill_chunk: at most %d chunks per call", kMaxBatch);
+    return PA_ERR_UNSUPPORTED;
+  }
+  if (num_pages * kPage >= (int64_t(1) << 31) || total_q >= (1 << 24)) return PA_ERR_UNSUPPORTED;
+  const int grid = sm_count_current_device();
+  if (grid <= 0) return PA_ERR_CUDA;
+  const PrefillWs w = prefill_ws(batch, grid);
+  if (workspace == nullptr || workspace_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
   CUtensorMap qm, km, vm;
   if (!make_map(&qm, q, static_cast<uint64_t>(total_q), kHq, kTileM) ||
       !make_map(&km, k_pool, static_cast<uint64_t>(num_pages) * kPage, kHkv, kPage) ||
@@ -432,6 +769,16 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(prefill_tc)");
+    // The in-kernel register split needs the full launch budget; a build that launched with
+    // fewer registers per thread would make setmaxnreg.inc wait forever, so refuse to launch.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+    if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncGetAttributes(prefill_tc)");
+    if (fa.numRegs < kLaunchRegs) {
+      snprintf_error("prefill_tc_kernel built with %d registers/thread, needs %d for its split",
+                     fa.numRegs, kLaunchRegs);
+      return PA_ERR_UNSUPPORTED;
+    }
     configured_device = dev;
   }
   PrefillTcParams p;
@@ -439,14 +786,21 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   p.seq_lens = seq_lens;
   p.block_table = block_table;
   p.bt_stride = bt_stride;
+  p.batch = batch;
   p.num_pages = num_pages;
   p.scale_log2 = softmax_scale * kLog2e;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.status = status;
-  dim3 grid((max_q_len + kTileM - 1) / kTileM, kHkv, batch);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_header = reinterpret_cast<long long*>(ws + w.header);
+  p.ws_prefix = reinterpret_cast<long long*>(ws + w.prefix);
+  p.ws_records = ws + w.records;
   prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(qm, km, vm, p);
   PA_CHECK_LAUNCH("prefill_tc_kernel");
+  dim3 mgrid((max_q_len + kTileM - 1) / kTileM, kHkv, batch);
+  prefill_merge_kernel<<<mgrid, 256, 0, stream>>>(p);
+  PA_CHECK_LAUNCH("prefill_merge_kernel");
   return PA_OK;
 }
 
