@@ -17,8 +17,8 @@
 // Per 128-key tile j of a job:
 //   S_t = Q_t K_j^T         tcgen05.mma, A = Q_t (smem), B = K_j (smem), D = S_t (TMEM fp32)
 //   P_t = softmax part      4 warps per M tile, one thread per row: tcgen05.ld S_t, mask the
-//                           diagonal, exp2 (3/4 on the MUFU unit, 1/4 by a cubic on the FMA
-//                           pipe), row sum; P_t written back over S_t as bf16
+//                           diagonal, exp2 on the MUFU unit, row sum; P_t written back
+//                           over S_t as bf16
 //   O_t += P_t V_j          tcgen05.mma, A = P_t (TMEM), B = V_j (smem, MN-major), D = O_t
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 // Warp roles: 0-3 softmax of M tile 0, 4-7 softmax of M tile 1, 8 TMA producer, 9 MMA issuer,
@@ -53,6 +53,12 @@ constexpr uint32_t kBlockBytes = 128 * 128;  // 128 rows x 64 bf16 (one swizzled
 constexpr uint32_t kTileBytes = 2 * kBlockBytes;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxBatch = 1024;
+// Which of a row's 32 probability pairs per half tile take the FMA-pipe exp2 instead of the
+// MUFU unit. Measured on GB300: the MUFU unit keeps up on its own (all-MUFU was 8% faster
+// than a quarter on the FMA pipe), so none do by default.
+#ifndef PA_POLY_PAIR
+#define PA_POLY_PAIR(k) false
+#endif
 // Register split: the two softmax warpgroups grow to 216 registers per thread, the
 // producer/MMA warpgroup shrinks to 72; 256 * 216 + 128 * 72 = 64,512 = 384 threads x 168, the
 // budget the CTA is launched with (checked on the host before every launch).
@@ -505,9 +511,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           for (int c = 0; c < 128; ++c)
             if (k0 + c > qpos) sb[c] = 0xff800000u;  // -inf: key after this query
         }
-        float mx = -CUDART_INF_F;
+        // row max over 8 independent partial maxima (no 128-long dependency chain)
+        float pm[8];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sb[c]));
+        for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(sb[k]);
+#pragma unroll
+        for (int c = 8; c < 128; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(sb[c]));
+        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
         const float mx2 = mx * p.scale_log2;
         const bool grow = mx2 > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, grow)) {
@@ -537,7 +548,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // then gives exp2(-inf) = 0 for its masked scores instead of NaN.
         const float m_eff = (m_used == -CUDART_INF_F) ? 0.f : m_used;
         const float2 nm2 = make_float2(-m_eff, -m_eff);
-        float2 lsum = make_float2(0.f, 0.f);
+        float2 ls[4];  // 4 independent paired partial sums
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t pk[32];
@@ -546,17 +559,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             const float2 x = fma2(make_float2(__uint_as_float(sb[c * 64 + 2 * k]),
                                               __uint_as_float(sb[c * 64 + 2 * k + 1])), sc2, nm2);
             float2 e;
-            if ((k & 3) == 3) {
+            if (PA_POLY_PAIR(k)) {
               e = exp2_poly2(x);
             } else {
               e.x = fast_exp2(x.x);
               e.y = fast_exp2(x.y);
             }
-            lsum = add2(lsum, e);
+            ls[k & 3] = add2(ls[k & 3], e);
             pk[k] = pack_bf16x2(e.x, e.y);
           }
           tc::tmem_st32(t_s + c * 32, pk);
         }
+        const float2 lsum = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
         l += lsum.x + lsum.y;
         tc::tmem_wait_st();
         tc::fence_before_sync();
