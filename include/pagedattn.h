@@ -159,12 +159,15 @@ pa_status attn_decode_paged_noalloc(pa_dims dims, const void* q, const void* k_p
  *   q           bf16 [total_q][Hq][128], chunks packed by sequence
  *   cu_q_lens   int32 [batch+1]: chunk b owns rows cu_q_lens[b] .. cu_q_lens[b+1]-1
  *   seq_lens    int32 [batch]: keys of sequence b INCLUDING the chunk (appended first)
- *   max_q_len   host upper bound of the chunk lengths (grid size)
+ *   batch       number of chunks, at most 128 per call
+ *   max_q_len   host upper bound of the chunk lengths
  * Query i of chunk b (length n) sits at position seq_lens[b] - n + i and sees keys
  * 0 .. seq_lens[b] - n + i (bottom-right causal alignment). A chunk longer than its sequence
  * is flagged and produces nothing.
  *   out bf16 [total_q][Hq][128]; lse fp32 [total_q][Hq] or NULL.
- *   workspace: pa_prefill_workspace_size(...) bytes (may be 0 / NULL when that is 0).
+ *   workspace: at least pa_prefill_workspace_size(...) bytes, 256-byte aligned (split-work
+ *   partials; about 40 MB on a 152-SM GPU, independent of the batch). Calls that share a
+ *   workspace must not overlap on the GPU.
  * ------------------------------------------------------------------------------------------ */
 size_t pa_prefill_workspace_size(pa_dims dims, int32_t batch, int32_t max_q_len,
                                  int32_t max_seq_len);

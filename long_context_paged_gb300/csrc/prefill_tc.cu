@@ -21,8 +21,9 @@
 //                           over S_t as bf16
 //   O_t += P_t V_j          tcgen05.mma, A = P_t (TMEM), B = V_j (smem, MN-major), D = O_t
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
-// Warp roles: 0-3 softmax of M tile 0, 4-7 softmax of M tile 1, 8 TMA producer, 9 MMA issuer,
-// 10-11 idle (they complete the third warpgroup, which gives its registers to the softmax).
+// Warp roles: 0-3 softmax of M tile 0, 4-7 softmax of M tile 1, 8 TMA producer of V, 9 MMA
+// issuer, 10 TMA producer of Q and K, 11 idle (it completes the third warpgroup, which gives
+// its registers to the softmax).
 // K/V tiles arrive by tiled TMA straight from the page pools: one 16-token page x 64 dims per
 // copy (a 3-D tensor map over [tokens][kv heads][dims] with 128-byte swizzle), so the block
 // table is applied per page without a gather pass. Pages past the sequence are fetched at an
@@ -47,15 +48,20 @@ namespace {
 constexpr int kTileM = 128;   // queries per job (per head)
 constexpr int kTileN = 128;   // keys per K/V tile
 constexpr int kThreads = 384; // 8 softmax warps + producer + MMA + 2 spare (3 warpgroups)
-constexpr int kProducerWarp = 8;
+constexpr int kProducerWarp = 8;   // V tiles
 constexpr int kMmaWarp = 9;
+constexpr int kKProducerWarp = 10; // Q and K tiles
 constexpr uint32_t kBlockBytes = 128 * 128;  // 128 rows x 64 bf16 (one swizzled 64-dim block)
 constexpr uint32_t kTileBytes = 2 * kBlockBytes;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kMaxBatch = 1024;
+constexpr int kMaxBatch = 128;   // chunks per call (the unit prefix lives in shared memory)
+constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more stage in flight
 // Which of a row's 32 probability pairs per half tile take the FMA-pipe exp2 instead of the
 // MUFU unit. Measured on GB300: the MUFU unit keeps up on its own (all-MUFU was 8% faster
 // than a quarter on the FMA pipe), so none do by default.
+#ifndef PA_L2_PREFETCH
+#define PA_L2_PREFETCH 1
+#endif
 #ifndef PA_POLY_PAIR
 #define PA_POLY_PAIR(k) false
 #endif
@@ -69,13 +75,13 @@ constexpr int kLaunchRegs = (256 * kSoftmaxRegs + 128 * kControlRegs) / kThreads
 constexpr size_t kRecordO = 2 * 128 * 128 * sizeof(float);
 constexpr size_t kRecordBytes = kRecordO + 2 * 128 * sizeof(float);
 
-struct __align__(1024) PrefillTcSmem {
+struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
   uint8_t q[2][2][kBlockBytes];   // [M tile][64-dim block]
   uint8_t k[2][2][kBlockBytes];   // [stage][64-dim block]
-  uint8_t v[2][2][kBlockBytes];
+  uint8_t v[kVStages][2][kBlockBytes];
   uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[2], v_empty[2];
+  uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -83,6 +89,8 @@ struct __align__(1024) PrefillTcSmem {
   long long total_units;
   long long unit_prefix[kMaxBatch + 1];  // first unit of each sequence
 };
+
+static_assert(sizeof(PrefillTcSmem) + 1024 <= 232448, "prefill shared memory over the 227 KB limit");
 
 struct PrefillTcParams {
   const int32_t* cu_q_lens;
@@ -278,12 +286,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
-      mbar_init(&s.v_full[i], 1);
-      mbar_init(&s.v_empty[i], 1);
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 128);
       mbar_init(&s.o_ready[i], 1);
       mbar_init(&s.o_free[i], 128);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_empty[i], 1);
     }
     mbar_init(&s.mma_done, 1);
     fence_mbar_init();
@@ -299,8 +309,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 
   if (warp >= 8) {
     tc::regs_decrease<kControlRegs>();
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ TMA producer
+  if (warp == kProducerWarp || warp == kKProducerWarp) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 10 loads Q and the K tiles, warp 8 the V tiles, each as soon as its own ring has a
+    // free stage (K is needed a whole P*V earlier than V). Each also prefetches the pages of
+    // the tile two ahead into L2.
+    const bool is_k = warp == kKProducerWarp;
+    const CUtensorMap* map = is_k ? &k_map : &v_map;
+    uint8_t(*ring)[2][kBlockBytes] = is_k ? s.k : s.v;
+    const uint32_t nst = is_k ? 2u : static_cast<uint32_t>(kVStages);
+    uint64_t* full = is_k ? s.k_full : s.v_full;
+    uint64_t* empty = is_k ? s.k_empty : s.v_empty;
     const int oob_token = static_cast<int>(p.num_pages * kPage);  // zero-filled coordinate
     bool ok = true;
     uint32_t it = 0, jc = 0;
@@ -321,56 +340,50 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         }
         return tok;
       };
-      int tok = page_token(pc.jb);
-      if (lane == 0) {
-        ok = wait_or_flag(&s.q_empty, (jc & 1) ^ 1u, p.status);
-        if (ok) {
-          mbar_arrive_expect_tx(&s.q_full, 4 * kBlockBytes);
-          for (int t = 0; t < 2; ++t)
-            for (int kb = 0; kb < 2; ++kb)
-              tc::tma_load_3d(s.q[t][kb], &q_map, kb * 64, 2 * pc.g + t,
-                              pc.s.q0 + pc.qt * kTileM, &s.q_full);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      for (int j = pc.jb; j < pc.je && ok; ++j, ++it) {
-        const int st = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        const int tok_next = (j + 1 < pc.je) ? page_token(j + 1) : 0;
-        if (lane == 0) ok = wait_or_flag(&s.k_empty[st], ph ^ 1u, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
-#pragma unroll
-        for (int pg = 0; pg < kTileN / kPage; ++pg) {
-          const int t = __shfl_sync(0xffffffffu, tok, pg);
-          if (lane == 0) {
-            tc::tma_load_3d(s.k[st][0] + pg * 2048, &k_map, 0, pc.g, t, &s.k_full[st]);
-            tc::tma_load_3d(s.k[st][1] + pg * 2048, &k_map, 64, pc.g, t, &s.k_full[st]);
+      if (is_k) {
+        if (lane == 0) {
+          ok = wait_or_flag(&s.q_empty, (jc & 1) ^ 1u, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&s.q_full, 4 * kBlockBytes);
+            for (int t = 0; t < 2; ++t)
+              for (int kb = 0; kb < 2; ++kb)
+                tc::tma_load_3d(s.q[t][kb], &q_map, kb * 64, 2 * pc.g + t,
+                                pc.s.q0 + pc.qt * kTileM, &s.q_full);
           }
         }
-        if (lane == 0) ok = wait_or_flag(&s.v_empty[st], ph ^ 1u, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      int tok = page_token(pc.jb);
+      int tok_next = (pc.jb + 1 < pc.je) ? page_token(pc.jb + 1) : oob_token;
+      for (int j = pc.jb; j < pc.je && ok; ++j, ++it) {
+        const int st = it % nst;
+        const uint32_t ph = (it / nst) & 1;
+        const int tok_ahead = (j + 2 < pc.je) ? page_token(j + 2) : oob_token;
+        if (PA_L2_PREFETCH && lane < kTileN / kPage && tok_ahead != oob_token) {
+          tc::tma_prefetch_3d(map, 0, pc.g, tok_ahead);
+          tc::tma_prefetch_3d(map, 64, pc.g, tok_ahead);
+        }
+        if (lane == 0) ok = wait_or_flag(&empty[st], ph ^ 1u, p.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
 #pragma unroll
         for (int pg = 0; pg < kTileN / kPage; ++pg) {
           const int t = __shfl_sync(0xffffffffu, tok, pg);
           if (lane == 0) {
-            tc::tma_load_3d(s.v[st][0] + pg * 2048, &v_map, 0, pc.g, t, &s.v_full[st]);
-            tc::tma_load_3d(s.v[st][1] + pg * 2048, &v_map, 64, pc.g, t, &s.v_full[st]);
+            tc::tma_load_3d(ring[st][0] + pg * 2048, map, 0, pc.g, t, &full[st]);
+            tc::tma_load_3d(ring[st][1] + pg * 2048, map, 64, pc.g, t, &full[st]);
           }
         }
         tok = tok_next;
+        tok_next = tok_ahead;
       }
       ++jc;
     }
     // do not leave while copies into this CTA's shared memory may still be landing
     if (lane == 0 && it > 0) {
-      for (uint32_t k = (it >= 2 ? it - 2 : 0); k < it; ++k) {
-        wait_or_flag(&s.k_full[k & 1], (k >> 1) & 1, p.status);
-        wait_or_flag(&s.v_full[k & 1], (k >> 1) & 1, p.status);
-      }
+      for (uint32_t k = (it >= nst ? it - nst : 0); k < it; ++k)
+        wait_or_flag(&full[k % nst], (k / nst) & 1, p.status);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -417,8 +430,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int i = 0; i < nt && ok; ++i) {
         const uint32_t cur = it + i;
-        const int st = cur & 1;
-        if (lane == 0) ok = wait_or_flag(&s.v_full[st], (cur >> 1) & 1, p.status);
+        const int st = cur & 1;                 // K stage
+        const int vst = cur % kVStages;         // V stage
+        if (lane == 0) ok = wait_or_flag(&s.v_full[vst], (cur / kVStages) & 1, p.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const int first_bad = pc.s.L - (pc.jb + i) * kTileN;  // V rows from here are not keys
@@ -427,7 +441,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           const int r0 = max(first_bad, 0);
           for (int e = r0 * 16 + lane; e < kTileN * 16; e += 32) {
             const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
-            *reinterpret_cast<uint4*>(s.v[st][c >> 3] + r * 128 + (c & 7) * 16) =
+            *reinterpret_cast<uint4*>(s.v[vst][c >> 3] + r * 128 + (c & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           tc::fence_proxy_async_smem();
@@ -439,7 +453,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           if (ok && i == 0 && jc > 0) ok = wait_or_flag(&s.o_free[0], (jc - 1) & 1, p.status);
           if (ok) {
             tc::fence_after_sync();
-            issue_pv(0, st, i > 0);
+            issue_pv(0, vst, i > 0);
             tc::mma_commit(&s.o_ready[0]);
             if (i + 1 < nt) {
               ok = wait_or_flag(&s.k_full[st1], ((cur + 1) >> 1) & 1, p.status);
@@ -454,9 +468,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           if (ok && i == 0 && jc > 0) ok = wait_or_flag(&s.o_free[1], (jc - 1) & 1, p.status);
           if (ok) {
             tc::fence_after_sync();
-            issue_pv(1, st, i > 0);
+            issue_pv(1, vst, i > 0);
             tc::mma_commit(&s.o_ready[1]);
-            tc::mma_commit(&s.v_empty[st]);
+            tc::mma_commit(&s.v_empty[vst]);
             if (i + 1 < nt) {
               issue_s(1, st1);
               tc::mma_commit(&s.s_full[1]);
