@@ -383,6 +383,20 @@ def capture(step: Step, parts):
     return g
 
 
+def max_over_ranks(dist, values, device):
+    """Element-wise maximum of per-rank timings (every rank gets the result)."""
+    if dist is None:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def weak_scaling_rate(units_per_rank, n_ranks, seconds):
+    """Whole-job throughput: every rank processed units_per_rank in at most `seconds`."""
+    return units_per_rank * n_ranks / seconds
+
+
 def timed_replays(graph, steps, warmup, dist):
     for _ in range(warmup):
         graph.replay()
@@ -456,15 +470,12 @@ def main():
     if has_dec and not has_pf and not step.append:
         t_dec = total_s
     clocks = sampler.stop(device_uuid()) if rank == 0 else None
-    if dist is not None:
-        t = torch.tensor([total_s, t_dec, t_pf], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s, t_dec, t_pf = t.tolist()
+    total_s, t_dec, t_pf = max_over_ranks(dist, [total_s, t_dec, t_pf], dev)
     n = world
     launches = K_ * (step.launches_per_step + (2 * step.layers if g_dec is not None else 0)
                      + (step.layers if g_pf is not None else 0))
-    dec_gbs = step.dec_bytes * step.layers * K_ * n / t_dec / 1e9 if t_dec else None
-    pf_tflops = step.pf_flops * step.layers * K_ * n / t_pf / 1e12 if t_pf else None
+    dec_gbs = weak_scaling_rate(step.dec_bytes * step.layers * K_, n, t_dec) / 1e9 if t_dec else None
+    pf_tflops = weak_scaling_rate(step.pf_flops * step.layers * K_, n, t_pf) / 1e12 if t_pf else None
 
     if pa.read_device_status(step.status):
         raise RuntimeError("device status flagged errors in the timed region")

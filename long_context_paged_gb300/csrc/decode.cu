@@ -39,6 +39,7 @@ constexpr int kStages = 3;
 constexpr uint32_t kPageBytes = kPage * kHkv * kHeadDim * 2;  // K (or V) of one page
 constexpr int kMaxBatch = 4096;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMinPagesPerCta = 4;
 
 struct DecodeSmem {
   uint8_t kv[kStages][2][kPageBytes];
@@ -142,7 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
   build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
 
   const int total = s.total;
-  const int W = (total + gridDim.x - 1) / gridDim.x;
+  // pages per CTA: an equal share, but at least kMinPagesPerCta so that short batches are not
+  // cut into one-page pieces whose partials would then all need merging
+  const int W = max((total + gridDim.x - 1) / gridDim.x, kMinPagesPerCta);
   if (blockIdx.x == 0) {
     if (tid == 0) {
       p.ws_header[0] = W;
@@ -415,6 +418,7 @@ __global__ void __launch_bounds__(kHq * 32) decode_merge_kernel(const DecodePara
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float sum = 0.f;
+#pragma unroll 4
   for (int c = c0; c <= c1; ++c) {
     const int64_t r = static_cast<int64_t>(b) + c;
     const float w = fast_exp2((p.ws_lse[r * kHq + h] - m) * kLog2e);
