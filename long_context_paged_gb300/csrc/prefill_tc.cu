@@ -8,10 +8,12 @@
 //
 // Work decomposition. A job is 128 queries of one chunk x both query heads of one KV head
 // (GQA 16/8): two 128-row M tiles that share every K/V tile read. A job's causal key range is
-// J tiles of 128 keys; one (job, key tile) pair is a unit. Units of all jobs are laid end to
-// end (sequence, then KV head, then query tile) and a persistent grid of one CTA per SM takes
-// equal contiguous unit ranges, so the work is balanced to one tile whatever the chunk
-// lengths and offsets. A job cut by range boundaries leaves normalised partial results
+// J tiles of 128 keys; one (job, key tile) pair is a unit. Jobs are ordered sequence, then KV
+// head, then query tile. A persistent grid of one CTA per SM first runs whole jobs round-robin
+// (CTA c takes jobs c, c + G, ...; all CTAs of a round start at key tile 0 together, so the CTAs
+// of a KV head read the same K/V tiles from L2), then splits the units of the remaining jobs
+// into equal contiguous ranges, so the work stays balanced to about one tile whatever the
+// chunk lengths and offsets. A job cut by range boundaries leaves normalised partial results
 // (o, lse) in the workspace; prefill_merge_kernel combines them by log-sum-exp.
 //
 // Per 128-key tile j of a job:
@@ -59,8 +61,10 @@ constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more 
 // Which of a row's 32 probability pairs per half tile take the FMA-pipe exp2 instead of the
 // MUFU unit. Measured on GB300: the MUFU unit keeps up on its own (all-MUFU was 8% faster
 // than a quarter on the FMA pipe), so none do by default.
+// L2 prefetch of the tile two ahead: off, since the round-robin schedule already keeps the
+// concurrently read K/V tiles in L2 and the extra copies cost more than they save (measured).
 #ifndef PA_L2_PREFETCH
-#define PA_L2_PREFETCH 1
+#define PA_L2_PREFETCH 0
 #endif
 #ifndef PA_POLY_PAIR
 #define PA_POLY_PAIR(k) false
@@ -88,6 +92,8 @@ struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
   long long warp_sums[kThreads / 32];
   long long total_units;
   long long unit_prefix[kMaxBatch + 1];  // first unit of each sequence
+  int32_t job_prefix[kMaxBatch + 1];     // first job of each sequence
+  int32_t total_jobs;
 };
 
 static_assert(sizeof(PrefillTcSmem) + 1024 <= 232448, "prefill shared memory over the 227 KB limit");
@@ -103,8 +109,10 @@ struct PrefillTcParams {
   uint16_t* out;
   float* lse;
   int32_t* status;
-  long long* ws_header;   // [0] units per CTA, [1] total units
-  long long* ws_prefix;   // [batch + 1]
+  long long* ws_header;   // [0] tail units per CTA, [1] total units, [2] first tail unit,
+                          // [3] jobs done whole in the round-robin phase
+  long long* ws_prefix;   // [batch + 1] first unit of each sequence
+  int32_t* ws_job_prefix; // [batch + 1] first job of each sequence
   uint8_t* ws_records;    // [2 * grid][kRecordBytes]
 };
 
@@ -153,10 +161,17 @@ struct Piece {
   bool valid;
 };
 
+// The pieces one CTA owns, in order: first whole jobs c, c + G, c + 2G, ... (G = grid size) for
+// `rounds` rounds, all CTAs starting at key tile 0 together so that the CTAs of one KV head stream
+// the same K/V tiles through L2 at about the same time; then an equal share [U0, U1) of the
+// units of the remaining jobs, whose first and last pieces may be parts of jobs shared with
+// neighbouring CTAs.
 struct JobWalker {
   const PrefillTcParams* p;
   const long long* prefix;
+  const int32_t* jprefix;
   long long U0, U1;
+  int rounds, round, G;
   Piece cur;
 
   __device__ void set(int b, int g, int qt, long long u0, const SeqGeom& s) {
@@ -171,27 +186,65 @@ struct JobWalker {
     cur.valid = u0 < U1 && cur.jb < cur.je;
   }
 
-  __device__ void start(const PrefillTcParams& pp, const long long* pre, long long u_begin,
-                        long long u_end) {
-    p = &pp;
-    prefix = pre;
-    U0 = u_begin;
-    U1 = u_end;
-    int lo = 0, hi = pp.batch;  // last b with prefix[b] <= U0 < prefix[b+1]
+  __device__ void set_whole_job(int jo) {
+    int lo = 0, hi = p->batch;  // last b with jprefix[b] <= jo < jprefix[b+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (pre[mid] <= U0) lo = mid; else hi = mid;
+      if (jprefix[mid] <= jo) lo = mid; else hi = mid;
     }
-    const SeqGeom s = seq_geom(pp, lo, false);
-    const long long rem = U0 - pre[lo];
+    const SeqGeom s = seq_geom(*p, lo, false);
+    const int rem = jo - jprefix[lo];
+    const int g = rem / s.nqt, qt = rem - g * s.nqt;
+    cur.b = lo;
+    cur.g = g;
+    cur.qt = qt;
+    cur.s = s;
+    cur.u0 = prefix[lo] + g * s.T + units_before(s, qt);
+    cur.J = static_cast<int>(tiles_of(s, qt));
+    cur.jb = 0;
+    cur.je = cur.J;
+    cur.valid = true;
+  }
+
+  __device__ void start_tail() {
+    if (U0 >= U1) {
+      cur.valid = false;
+      return;
+    }
+    int lo = 0, hi = p->batch;  // last b with prefix[b] <= U0 < prefix[b+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= U0) lo = mid; else hi = mid;
+    }
+    const SeqGeom s = seq_geom(*p, lo, false);
+    const long long rem = U0 - prefix[lo];
     const int g = static_cast<int>(rem / s.T);
     const long long rem2 = rem - g * s.T;
     int qt = 0;
     while (qt + 1 < s.nqt && units_before(s, qt + 1) <= rem2) ++qt;
-    set(lo, g, qt, pre[lo] + g * s.T + units_before(s, qt), s);
+    set(lo, g, qt, prefix[lo] + g * s.T + units_before(s, qt), s);
+  }
+
+  __device__ void start(const PrefillTcParams& pp, const long long* pre, const int32_t* jpre,
+                        int n_rounds, int grid, long long u_begin, long long u_end) {
+    p = &pp;
+    prefix = pre;
+    jprefix = jpre;
+    U0 = u_begin;
+    U1 = u_end;
+    rounds = n_rounds;
+    G = grid;
+    round = 0;
+    if (rounds > 0) set_whole_job(static_cast<int>(blockIdx.x));
+    else start_tail();
   }
 
   __device__ void next() {
+    if (round < rounds) {
+      if (++round < rounds) set_whole_job(static_cast<int>(blockIdx.x) + round * G);
+      else start_tail();
+      return;
+    }
     long long u0 = cur.u0 + cur.J;
     int b = cur.b, g = cur.g, qt = cur.qt + 1;
     SeqGeom s = cur.s;
@@ -235,8 +288,14 @@ __device__ void build_unit_prefix(const PrefillTcParams& p, PrefillTcSmem& s) {
   const int per = (p.batch + kThreads - 1) / kThreads;
   const int b0 = min(p.batch, tid * per), b1 = min(p.batch, b0 + per);
   long long local = 0;
-  for (int b = b0; b < b1; ++b) local += kHkv * seq_geom(p, b, blockIdx.x == 0).T;
-  const long long incl = warp_incl_scan64(local, lane);
+  int local_jobs = 0;
+  for (int b = b0; b < b1; ++b) {
+    const SeqGeom g = seq_geom(p, b, blockIdx.x == 0);
+    local += kHkv * g.T;
+    local_jobs += kHkv * g.nqt;
+  }
+  const long long incl = warp_incl_scan64((static_cast<long long>(local_jobs) << 40) | local, lane);
+  // (jobs in the top 24 bits, units in the low 40: both sums fit: units < 2^40, jobs < 2^23)
   if (lane == 31) s.warp_sums[warp] = incl;
   __syncthreads();
   if (tid == 0) {
@@ -249,12 +308,23 @@ __device__ void build_unit_prefix(const PrefillTcParams& p, PrefillTcSmem& s) {
     s.total_units = run;
   }
   __syncthreads();
-  long long run = s.warp_sums[warp] + incl - local;
+  const long long packed = s.warp_sums[warp] + incl - ((static_cast<long long>(local_jobs) << 40) | local);
+  long long run = packed & ((1ll << 40) - 1);
+  int jrun = static_cast<int>(packed >> 40);
   for (int b = b0; b < b1; ++b) {
+    const SeqGeom g = seq_geom(p, b, false);
     s.unit_prefix[b] = run;
-    run += kHkv * seq_geom(p, b, false).T;
+    s.job_prefix[b] = jrun;
+    run += kHkv * g.T;
+    jrun += kHkv * g.nqt;
   }
-  if (tid == 0) s.unit_prefix[p.batch] = s.total_units;
+  __syncthreads();
+  if (tid == 0) {
+    s.total_jobs = static_cast<int>(s.total_units >> 40);
+    s.total_units &= (1ll << 40) - 1;
+    s.unit_prefix[p.batch] = s.total_units;
+    s.job_prefix[p.batch] = s.total_jobs;
+  }
   __syncthreads();
 }
 
@@ -269,16 +339,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 
   build_unit_prefix(p, s);
   const long long total = s.total_units;
-  const long long W = (total + gridDim.x - 1) / gridDim.x;
+  const int G = gridDim.x;
+  const int rounds = s.total_jobs / G;            // whole-job rounds (every CTA one job each)
+  const int n_dp = rounds * G;
+  long long T0 = total;                           // first unit of job n_dp
+  if (n_dp < s.total_jobs) {
+    int lo = 0, hi = p.batch;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s.job_prefix[mid] <= n_dp) lo = mid; else hi = mid;
+    }
+    const SeqGeom g0 = seq_geom(p, lo, false);
+    const int rem = n_dp - s.job_prefix[lo];
+    T0 = s.unit_prefix[lo] + (rem / g0.nqt) * g0.T + units_before(g0, rem % g0.nqt);
+  }
+  const long long Wt = (total - T0 + G - 1) / G;  // tail units per CTA
   if (blockIdx.x == 0) {
     if (threadIdx.x == 0) {
-      p.ws_header[0] = W;
+      p.ws_header[0] = Wt;
       p.ws_header[1] = total;
+      p.ws_header[2] = T0;
+      p.ws_header[3] = n_dp;
     }
-    for (int b = threadIdx.x; b <= p.batch; b += kThreads) p.ws_prefix[b] = s.unit_prefix[b];
+    for (int b = threadIdx.x; b <= p.batch; b += kThreads) {
+      p.ws_prefix[b] = s.unit_prefix[b];
+      p.ws_job_prefix[b] = s.job_prefix[b];
+    }
   }
-  const long long U0 = blockIdx.x * W, U1 = min(total, U0 + W);
-  if (U0 >= U1) return;  // uniform across the CTA: nothing allocated yet
+  const long long U0 = T0 + blockIdx.x * Wt, U1 = min(total, U0 + Wt);
+  if (rounds == 0 && U0 >= U1) return;  // uniform across the CTA: nothing allocated yet
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
@@ -305,15 +394,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   const uint32_t tmem = s.tmem_base;
 
   JobWalker jw;
-  jw.start(p, s.unit_prefix, U0, U1);
+  jw.start(p, s.unit_prefix, s.job_prefix, rounds, G, U0, U1);
 
   if (warp >= 8) {
     tc::regs_decrease<kControlRegs>();
   if (warp == kProducerWarp || warp == kKProducerWarp) {
     // ------------------------------------------------------------------ TMA producers
     // Warp 10 loads Q and the K tiles, warp 8 the V tiles, each as soon as its own ring has a
-    // free stage (K is needed a whole P*V earlier than V). Each also prefetches the pages of
-    // the tile two ahead into L2.
+    // free stage (K is needed a whole P*V earlier than V).
     const bool is_k = warp == kKProducerWarp;
     const CUtensorMap* map = is_k ? &k_map : &v_map;
     uint8_t(*ring)[2][kBlockBytes] = is_k ? s.k : s.v;
@@ -662,10 +750,12 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
   const int b = blockIdx.z, g = blockIdx.y, qt = blockIdx.x;
   const SeqGeom s = seq_geom(p, b, false);
   if (qt >= s.nqt) return;
-  const long long W = p.ws_header[0];
+  const int jo = p.ws_job_prefix[b] + g * s.nqt + qt;
+  if (jo < p.ws_header[3]) return;  // done whole in the round-robin phase
+  const long long Wt = p.ws_header[0], T0 = p.ws_header[2];
   const long long u0 = p.ws_prefix[b] + g * s.T + units_before(s, qt);
   const long long J = tiles_of(s, qt);
-  const long long c0 = u0 / W, c1 = (u0 + J - 1) / W;
+  const long long c0 = (u0 - T0) / Wt, c1 = (u0 + J - 1 - T0) / Wt;
   if (c0 == c1) return;
   const int t = threadIdx.x >> 7, r = threadIdx.x & 127;
   const int qrow = qt * kTileM + r;
@@ -746,14 +836,15 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t outer, uint64_t heads
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct PrefillWs {
-  size_t header, prefix, records, total;
+  size_t header, prefix, job_prefix, records, total;
 };
 
 PrefillWs prefill_ws(int batch, int grid) {
   PrefillWs w;
   w.header = 0;
   w.prefix = 256;
-  w.records = align256(w.prefix + sizeof(long long) * (batch + 1));
+  w.job_prefix = align256(w.prefix + sizeof(long long) * (batch + 1));
+  w.records = align256(w.job_prefix + sizeof(int32_t) * (batch + 1));
   w.total = align256(w.records + 2 * static_cast<size_t>(grid) * kRecordBytes);
   return w;
 }
@@ -823,6 +914,7 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_header = reinterpret_cast<long long*>(ws + w.header);
   p.ws_prefix = reinterpret_cast<long long*>(ws + w.prefix);
+  p.ws_job_prefix = reinterpret_cast<int32_t*>(ws + w.job_prefix);
   p.ws_records = ws + w.records;
   prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(qm, km, vm, p);
   PA_CHECK_LAUNCH("prefill_tc_kernel");
