@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
     }
     fence_mbar_init();
   }
+  // the merge kernel only reads this grid's results after griddepcontrol.wait (full completion),
+  // so it may be launched as soon as every CTA of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;");
   build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
 
   const int total = s.total;
@@ -399,7 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
 
 // Merge the partial results of sequences that crossed a CTA range boundary; also writes the
 // result of empty sequences (o = 0, lse = -inf). One CTA per sequence, one warp per head.
+// Launched as a programmatic dependent of decode_splitkv_kernel: its CTAs may start while the
+// split kernel is still running and wait (griddepcontrol.wait) until that grid has completed
+// and its writes are visible, which hides this launch behind the split kernel.
 __global__ void __launch_bounds__(kHq * 32) decode_merge_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x;
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p0 = p.ws_prefix[b], p1 = p.ws_prefix[b + 1];
@@ -417,19 +424,28 @@ __global__ void __launch_bounds__(kHq * 32) decode_merge_kernel(const DecodePara
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float sum = 0.f;
-#pragma unroll 4
-  for (int c = c0; c <= c1; ++c) {
-    const int64_t r = static_cast<int64_t>(b) + c;
-    const float w = fast_exp2((p.ws_lse[r * kHq + h] - m) * kLog2e);
-    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + (r * kHq + h) * kHeadDim + 4 * lane);
-    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-    sum += w;
+  float wsum = 0.f;
+  for (int base = c0; base <= c1; base += 32) {
+    // lane k owns the weight of part base + k; every lane then loads its 4 dims of each part
+    const int c = base + lane;
+    const float w = c <= c1
+        ? fast_exp2((p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h] - m) * kLog2e) : 0.f;
+    wsum += w;
+    const int n = min(32, c1 - base + 1);
+    const float* src = p.ws_o + ((static_cast<int64_t>(b) + base) * kHq + h) * kHeadDim + 4 * lane;
+#pragma unroll 8
+    for (int k = 0; k < n; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      const float4 o = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(k) * kHq * kHeadDim);
+      acc.x += wk * o.x; acc.y += wk * o.y; acc.z += wk * o.z; acc.w += wk * o.w;
+    }
   }
-  const float inv = 1.0f / sum;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  const float inv = 1.0f / wsum;
   *reinterpret_cast<uint2*>(orow) =
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = m + logf(sum);
+  if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = m + logf(wsum);
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -527,8 +543,20 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   decode_splitkv_kernel<<<grid, kThreads, sizeof(DecodeSmem), st>>>(p);
   PA_CHECK_LAUNCH("decode_splitkv_kernel");
-  decode_merge_kernel<<<batch, kHq * 32, 0, st>>>(p);
-  PA_CHECK_LAUNCH("decode_merge_kernel");
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(batch);
+    cfg.blockDim = dim3(kHq * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, p);
+    if (e != cudaSuccess) return record_cuda_error(e, "decode_merge_kernel");
+  }
   return PA_OK;
 }
 

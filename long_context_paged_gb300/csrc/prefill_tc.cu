@@ -337,6 +337,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   PrefillTcSmem& s = *reinterpret_cast<PrefillTcSmem*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  asm volatile("griddepcontrol.launch_dependents;");  // the merge kernel waits for completion
   build_unit_prefix(p, s);
   const long long total = s.total_units;
   const int G = gridDim.x;
@@ -747,6 +748,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 // Combine the pieces of jobs that were cut by CTA range boundaries. One CTA per job; thread =
 // (head, row). The pieces are slot 1 of the first CTA and slot 0 of each later CTA.
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParams p) {
+  // programmatic dependent of prefill_tc_kernel: wait until that grid is complete and visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.z, g = blockIdx.y, qt = blockIdx.x;
   const SeqGeom s = seq_geom(p, b, false);
   if (qt >= s.nqt) return;
@@ -918,9 +921,17 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   p.ws_records = ws + w.records;
   prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(qm, km, vm, p);
   PA_CHECK_LAUNCH("prefill_tc_kernel");
-  dim3 mgrid((max_q_len + kTileM - 1) / kTileM, kHkv, batch);
-  prefill_merge_kernel<<<mgrid, 256, 0, stream>>>(p);
-  PA_CHECK_LAUNCH("prefill_merge_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((max_q_len + kTileM - 1) / kTileM, kHkv, batch);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_merge_kernel, p);
+  if (e != cudaSuccess) return record_cuda_error(e, "prefill_merge_kernel");
   return PA_OK;
 }
 
