@@ -39,8 +39,17 @@ reordering of a row's reduction: a library matmul evaluates the score vectors of
 independent query rows of one (sequence, head) at once, then the definition above is applied
 to each row as written.
 
-Parity pins: every function here is pinned by tests in ``tests/test_oracle_pins.py`` against
-hand-worked fixtures (``tests/golden/``), closed forms, invariants and brute force.
+The audio-text bridge that feeds those embeddings to the decoder ("Optimizing ASR Models to
+Transcribe 90-Minute Multi-Speaker Audio", "ASR Model Primer", encoder bullet and component
+table; "MOSS-Transcribe-Diarize 0.9B", "Model Architecture": 4x temporal merge + MLP adaptor)
+concatenates every 4 consecutive encoder frames (d_model 1024 -> 4096) and applies
+Linear -> SiLU -> Linear -> LayerNorm down to 1024. The hidden width is not stated; the plainest
+reading, taken here, is Linear(4096 -> 1024), SiLU, Linear(1024 -> 1024), LayerNorm(1024) with
+a learned scale and shift.
+
+Parity pins: every function here is pinned by tests in ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_adaptor_pins.py`` against hand-worked fixtures (``tests/golden/``), closed
+forms, invariants, brute force and an independent library.
 """
 from __future__ import annotations
 
@@ -59,6 +68,8 @@ __all__ = [
     "prefill",
     "kv_append",
     "merge_lse",
+    "temporal_merge",
+    "adaptor",
 ]
 
 
@@ -268,3 +279,27 @@ def merge_lse(o_parts, lse_parts):
     o = np.where(any_part[..., None], contrib.sum(axis=0) / safe_total[..., None], 0.0)
     lse = np.where(any_part, m_safe + np.log(safe_total), -np.inf)
     return o, lse
+
+
+# ----------------------------------------------------------------------------------------------
+# Audio-text bridge: 4x temporal merge + adaptor MLP.
+# ----------------------------------------------------------------------------------------------
+def temporal_merge(frames, factor: int = 4):
+    """[T_enc, d] encoder frames -> [T_enc / factor, factor * d]: row t is frames
+    factor*t .. factor*t + factor - 1 laid side by side."""
+    frames = as_f64(frames)
+    T_enc, d = frames.shape
+    assert T_enc % factor == 0, "the frame count must be a multiple of the merge factor"
+    return np.concatenate([frames[k::factor] for k in range(factor)], axis=1)
+
+
+def adaptor(frames, w1, b1, w2, b2, gamma, beta, eps: float = 1e-5):
+    """Audio embeddings for the decoder: LayerNorm(SiLU(x W1^T + b1) W2^T + b2), x the
+    4x-merged frames. w1 [H, 4d], w2 [E, H] as (out, in); returns float64 [T, E]."""
+    x = temporal_merge(frames)
+    h = x @ as_f64(w1).T + as_f64(b1)
+    h = h / (1.0 + np.exp(-h))                       # SiLU(h) = h * sigmoid(h)
+    y = h @ as_f64(w2).T + as_f64(b2)
+    mu = y.mean(axis=1, keepdims=True)
+    var = ((y - mu) ** 2).mean(axis=1, keepdims=True)  # biased variance
+    return (y - mu) / np.sqrt(var + eps) * as_f64(gamma) + as_f64(beta)
