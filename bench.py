@@ -423,7 +423,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="mixed_28l", choices=sorted(W.CONFIG_SEED))
+    ap.add_argument("--workload", default="mixed_28l", choices=sorted(W.CONFIG_SEED) + ["adaptor_90min"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clocks-out", default=None)
@@ -444,6 +444,8 @@ def main():
     import long_context_paged_gb300 as pa
     pa.load()
     dev = f"cuda:{local}"
+    if args.workload == "adaptor_90min":
+        return run_adaptor(pa, args, dev, dist, world, rank)
     step = Step(pa, args.workload, dev)
     hbm, bf16, bf16s, peak_src = peaks()
 
@@ -563,6 +565,46 @@ def main():
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_adaptor(pa, args, dev, dist, world, rank):
+    """4x temporal merge + adaptor MLP for 90 minutes of audio (270,000 frames -> 67,500
+    embeddings): two tcgen05 GEMMs (4096 -> 1024 with SiLU, 1024 -> 1024) and a LayerNorm."""
+    n_frames = 270_000
+    inp = W.make_adaptor(W.ADAPTOR_SEED, n_frames, device=dev)
+    T = n_frames // 4
+    out = torch.empty(T, 1024, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(pa.adaptor_workspace_size(n_frames), dtype=torch.uint8, device=dev)
+    call = lambda: pa.adaptor_mlp_merge4(inp.frames, inp.w1, inp.b1, inp.w2, inp.b2, inp.gamma,
+                                         inp.beta, inp.eps, out=out, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    sampler = ClockSampler(args.clocks_out)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    t = timed_replays(g, args.steps, max(args.warmup, 0), dist)
+    clocks = sampler.stop(device_uuid()) if rank == 0 else None
+    (t,) = max_over_ranks(dist, [t], dev)
+    flops = 2.0 * T * 1024 * (4096 + 1024)
+    tflops = weak_scaling_rate(flops * args.steps, world, t) / 1e12
+    hbm, bf16, bf16s, peak_src = peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "adaptor (4x merge + Linear-SiLU-Linear-LayerNorm) TFLOP/s", "value": round(tflops, 1),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "adaptor_90min", "frames": n_frames, "tokens": T,
+                       "timing": "CUDA events around CUDA-graph replays of the call"},
+            "roofline": {"kernel": "gemm_bias_act (two GEMMs) + layernorm", "bound": "tensor",
+                         "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
+                         "frac": round(tflops / bf16, 4), "peak_source": f"{peak_src} bf16_tflops",
+                         "traffic": None, "algorithmic_flops_per_launch": flops},
+            "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
 
 
 def run_reference(args, world, rank):

@@ -198,6 +198,32 @@ pa_status attn_merge_lse(int32_t num_parts, int32_t rows, int32_t heads, int32_t
                          const float* o_parts, const float* lse_parts, void* out,
                          float* lse_out, pa_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * adaptor_mlp_merge4 — the audio-text bridge that turns encoder frames into decoder embeddings.
+ *
+ * Source: 4x temporal merge (concatenate every 4 encoder frames, d_model 1024 -> 4096) and an
+ * FFN adapter Linear -> SiLU -> Linear -> LayerNorm, 4096 -> 1024 ("Optimizing ASR Models to
+ * Transcribe 90-Minute Multi-Speaker Audio", "ASR Model Primer"; "MOSS-Transcribe-Diarize
+ * 0.9B", "Model Architecture"). The hidden width is not stated; it is 1024 here:
+ *     x = frames viewed as [T][4096] (T = num_frames / 4; no copy is made)
+ *     out = LayerNorm(SiLU(x W1^T + b1) W2^T + b2) * gamma + beta   (biased variance, eps)
+ *
+ *   frames   bf16 [num_frames][1024], num_frames a multiple of 4
+ *   w1       bf16 [1024][4096] (out, in);  b1 fp32 [1024]
+ *   w2       bf16 [1024][1024] (out, in);  b2 fp32 [1024]
+ *   gamma, beta  fp32 [1024];  eps >= 0
+ *   out      bf16 [T][1024]
+ *   workspace    at least pa_adaptor_workspace_size(num_frames) bytes (the bf16 hidden
+ *                activations, [T][1024]); 16-byte aligned.
+ * ------------------------------------------------------------------------------------------ */
+size_t pa_adaptor_workspace_size(int32_t num_frames);
+
+pa_status adaptor_mlp_merge4(int32_t num_frames, const void* frames, const void* w1,
+                             const float* b1, const void* w2, const float* b2,
+                             const float* gamma, const float* beta, float eps, void* out,
+                             void* workspace, size_t workspace_bytes, int32_t* status,
+                             pa_stream_t stream);
+
 /* Read and clear the device status word: waits for `stream`, copies *status to *flags_out,
  * then zeroes it. */
 pa_status pa_read_device_status(int32_t* status, uint32_t* flags_out, pa_stream_t stream);

@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "load", "PagedAttnError", "Dims", "DEFAULT_DIMS",
     "kv_append_paged", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_prefill_chunk",
-    "attn_merge_lse",
+    "attn_merge_lse", "adaptor_mlp_merge4", "adaptor_workspace_size",
     "decode_workspace_size", "prefill_workspace_size", "read_device_status",
     "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "lib_path",
 ]
@@ -72,6 +72,8 @@ _SIGS = {
     "attn_prefill_chunk": (_I32, [Dims, _P, _P, _I32, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
                                   _F, _P, _P, _P, _SZ, _P, _P]),
     "attn_merge_lse": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "pa_adaptor_workspace_size": (_SZ, [_I32]),
+    "adaptor_mlp_merge4": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _SZ, _P, _P]),
     "pa_read_device_status": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "pa_status_string": (ctypes.c_char_p, [_I32]),
     "pa_last_error": (ctypes.c_char_p, []),
@@ -251,6 +253,34 @@ def attn_merge_lse(o_parts, lse_parts, *, out=None, lse_out=None, stream=None):
     _check("attn_merge_lse", lib.attn_merge_lse(S, R, H, D, _ptr(o_parts), _ptr(lse_parts),
                                                 _ptr(out), _ptr(lse_out), _stream(stream)))
     return out, lse_out
+
+
+def adaptor_workspace_size(num_frames: int) -> int:
+    return int(load().pa_adaptor_workspace_size(num_frames))
+
+
+def adaptor_mlp_merge4(frames, w1, b1, w2, b2, gamma, beta, eps: float = 1e-5, *, out=None,
+                       workspace=None, status=None, stream=None):
+    """Decoder embeddings from encoder frames [T_enc, 1024]: 4x merge, Linear-SiLU-Linear-
+    LayerNorm. Returns out bf16 [T_enc / 4, 1024]."""
+    _need(frames, "frames", torch.bfloat16, 2)
+    _need(w1, "w1", torch.bfloat16, 2)
+    _need(w2, "w2", torch.bfloat16, 2)
+    for t, n in ((b1, "b1"), (b2, "b2"), (gamma, "gamma"), (beta, "beta")):
+        _need(t, n, torch.float32, 1)
+    n_frames = frames.shape[0]
+    T = n_frames // 4
+    if out is None:
+        out = torch.empty(T, 1024, dtype=torch.bfloat16, device=frames.device)
+    if workspace is None:
+        workspace = torch.empty(max(256, adaptor_workspace_size(n_frames)), dtype=torch.uint8,
+                                device=frames.device)
+    lib = load()
+    _check("adaptor_mlp_merge4", lib.adaptor_mlp_merge4(
+        n_frames, _ptr(frames), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), _ptr(gamma), _ptr(beta),
+        float(eps), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
+    return out
 
 
 def read_device_status(status, stream=None) -> int:

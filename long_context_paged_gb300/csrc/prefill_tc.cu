@@ -39,12 +39,14 @@
 #include <math_constants.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "pa_common.cuh"
 #include "tc_common.cuh"
 
 namespace pa {
+
+bool make_map_3d(CUtensorMap* map, const void* base, uint64_t outer, uint64_t heads,
+                 uint32_t box_rows);
+
 namespace {
 
 constexpr int kTileM = 128;   // queries per job (per head)
@@ -520,7 +522,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int i = 0; i < nt && ok; ++i) {
         const uint32_t cur = it + i;
-        const int st = cur & 1;                 // K stage
         const int vst = cur % kVStages;         // V stage
         if (lane == 0) ok = wait_or_flag(&s.v_full[vst], (cur / kVStages) & 1, p.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -808,35 +809,6 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
 // ---------------------------------------------------------------------------------------------
 // host side: tensor maps (driver entry point looked up once), workspace layout, launch
 // ---------------------------------------------------------------------------------------------
-std::once_flag g_encode_once;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode;
-}
-
-// 3-D bf16 view [outer][heads][128 dims] (dims innermost), box = 64 dims x 1 head x box_rows,
-// 128-byte swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* map, const void* base, uint64_t outer, uint64_t heads, uint32_t box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), heads, outer};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2), heads * kHeadDim * 2};
-  cuuint32_t box[3] = {64, 1, box_rows};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct PrefillWs {
@@ -878,9 +850,9 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   if (workspace == nullptr || workspace_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
   CUtensorMap qm, km, vm;
-  if (!make_map(&qm, q, static_cast<uint64_t>(total_q), kHq, kTileM) ||
-      !make_map(&km, k_pool, static_cast<uint64_t>(num_pages) * kPage, kHkv, kPage) ||
-      !make_map(&vm, v_pool, static_cast<uint64_t>(num_pages) * kPage, kHkv, kPage)) {
+  if (!make_map_3d(&qm, q, static_cast<uint64_t>(total_q), kHq, kTileM) ||
+      !make_map_3d(&km, k_pool, static_cast<uint64_t>(num_pages) * kPage, kHkv, kPage) ||
+      !make_map_3d(&vm, v_pool, static_cast<uint64_t>(num_pages) * kPage, kHkv, kPage)) {
     snprintf_error("cuTensorMapEncodeTiled failed for the prefill operands");
     return PA_ERR_CUDA;
   }

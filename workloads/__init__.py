@@ -226,3 +226,37 @@ def make_workload(name: str, *, device="cpu", poison=False, seed=None, **kw) -> 
 def kv_bytes_per_token(num_kv_heads: int = HKV, head_dim: int = HEAD_DIM) -> int:
     """K plus V bytes of one token in one layer (bf16)."""
     return 2 * num_kv_heads * head_dim * 2
+
+
+# ----------------------------------------------------------------------------------------------
+# Audio-text bridge inputs: encoder frames and synthetic adaptor weights.
+# ----------------------------------------------------------------------------------------------
+D_MODEL = 1024
+ADAPTOR_SEED = 1006
+
+
+@dataclass
+class AdaptorInputs:
+    """frames bf16 [T_enc, 1024]; w1 bf16 [1024, 4096]; w2 bf16 [1024, 1024] (out, in);
+    b1, b2, gamma, beta fp32 [1024]; eps."""
+    frames: torch.Tensor
+    w1: torch.Tensor
+    b1: torch.Tensor
+    w2: torch.Tensor
+    b2: torch.Tensor
+    gamma: torch.Tensor
+    beta: torch.Tensor
+    eps: float = 1e-5
+
+
+def make_adaptor(seed: int, num_frames: int, device="cpu") -> AdaptorInputs:
+    """Frames ~ N(0, 1) (post-LayerNorm encoder output scale); weights ~ N(0, 1/fan_in);
+    biases ~ N(0, 0.02^2); gamma ~ 1 + N(0, 0.1^2); beta ~ N(0, 0.1^2)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    r = lambda *shape: torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+    frames = _randn_bf16_chunked((num_frames, D_MODEL), g, device)
+    w1 = (r(1024, 4 * D_MODEL) / 64.0).to(torch.bfloat16)
+    w2 = (r(1024, 1024) / 32.0).to(torch.bfloat16)
+    return AdaptorInputs(frames=frames, w1=w1, b1=0.02 * r(1024), w2=w2, b2=0.02 * r(1024),
+                         gamma=1.0 + 0.1 * r(1024), beta=0.1 * r(1024))
