@@ -1,7 +1,7 @@
-"""Seeded synthetic inputs for paged GQA attention.
+"""Seeded synthetic inputs for paged GQA attention and the audio-text adaptor.
 
-This module is shared by the parity tests, the smoke check and the bench. It holds no
-attention arithmetic: only shapes, sequence lengths, page placement and random values. The
+This module is shared by the parity tests, the smoke check and the bench. It holds none of the
+method's arithmetic: only shapes, sequence lengths, page placement and random values. The
 oracle and the CUDA path both consume what it produces; neither is imported here.
 
 Workloads (sizes of the long-audio transcription setting: 12.5 encoder tokens per second of
