@@ -85,7 +85,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.acc_full[i], 1);
-      mbar_init(&s.acc_empty[i], 128);
+      mbar_init(&s.acc_empty[i], 4);  // one arrive per epilogue warp
     }
     mbar_init(&s.mma_done, 1);
     fence_mbar_init();
@@ -185,7 +185,8 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
         }
       }
       tc::fence_before_sync();
-      mbar_arrive(&s.acc_empty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.acc_empty[acc]);
     }
   }
 

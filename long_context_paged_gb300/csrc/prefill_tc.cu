@@ -74,8 +74,8 @@ constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more 
 // Register split: the two softmax warpgroups grow to 216 registers per thread, the
 // producer/MMA warpgroup shrinks to 72; 256 * 216 + 128 * 72 = 64,512 = 384 threads x 168, the
 // budget the CTA is launched with (checked on the host before every launch).
-constexpr int kSoftmaxRegs = 216;
-constexpr int kControlRegs = 72;
+constexpr int kSoftmaxRegs = 200;
+constexpr int kControlRegs = 104;
 constexpr int kLaunchRegs = (256 * kSoftmaxRegs + 128 * kControlRegs) / kThreads;
 // A partial result: o [2 heads][128 rows][128] fp32, then lse [2][128] fp32.
 constexpr size_t kRecordO = 2 * 128 * 128 * sizeof(float);
@@ -379,9 +379,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.p_full[i], 4);   // one arrive per softmax warp
       mbar_init(&s.o_ready[i], 1);
-      mbar_init(&s.o_free[i], 128);
+      mbar_init(&s.o_free[i], 4);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&s.v_full[i], 1);
@@ -480,102 +480,114 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
+    // The tensor pipe queues only about one instruction ahead of the issuing thread, so the
+    // work between two MMA groups shows up directly as idle pipe time. Lane 0 runs the whole
+    // loop alone (no per-tile warp collectives); ring stages and barrier parities are
+    // counters; descriptors are built once and selected, and a K step is a constant added to
+    // the start field (16-byte units; shared memory stays below 256 KB, so it cannot carry out
+    // of its 14 bits).
     constexpr uint32_t id_s = tc::idesc_bf16(128, kTileN, 0, 0);    // S = Q K^T
     constexpr uint32_t id_o = tc::idesc_bf16(128, 128, 0, 1);       // O = P V, V MN-major
-    auto issue_s = [&](int t, int st) {
-      const uint32_t qa = smem_addr(s.q[t][0]), kb = smem_addr(s.k[st][0]);
+    static_assert(kVStages == 3, "the V descriptor selection below assumes three stages");
+    if (lane == 0) {
+      const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(s.q[0][0]), 16, 1024);
+      const uint64_t dq1 = tc::smem_desc_sw128(smem_addr(s.q[1][0]), 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(s.k[0][0]), 16, 1024);
+      const uint64_t dk1 = tc::smem_desc_sw128(smem_addr(s.k[1][0]), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(s.v[0][0]), kBlockBytes, 1024);
+      const uint64_t dv1 = tc::smem_desc_sw128(smem_addr(s.v[1][0]), kBlockBytes, 1024);
+      const uint64_t dv2 = tc::smem_desc_sw128(smem_addr(s.v[2][0]), kBlockBytes, 1024);
+      auto issue_s = [&](uint32_t d, uint64_t a, uint64_t b) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off_b = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-        tc::mma_ss(tmem + t * 128, tc::smem_desc_sw128(qa + off_b, 16, 1024),
-                   tc::smem_desc_sw128(kb + off_b, 16, 1024), id_s, kk > 0);
-      }
-    };
-    auto issue_pv = [&](int t, int st, bool acc) {
-      const uint32_t vb = smem_addr(s.v[st][0]);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        tc::mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                   tc::smem_desc_sw128(vb + kk * 2048, kBlockBytes, 1024), id_o,
-                   (acc || kk > 0) ? 1u : 0u);
-      }
-    };
-    bool ok = true;
-    uint32_t it = 0, jc = 0;
-    for (; jw.cur.valid && ok; jw.next()) {
-      const Piece& pc = jw.cur;
-      const int nt = pc.je - pc.jb;
-      if (lane == 0) {
-        const int st = it & 1;
-        ok = wait_or_flag(&s.q_full, jc & 1, p.status) &&
-             wait_or_flag(&s.k_full[st], (it >> 1) & 1, p.status);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_s(0, st);
-          tc::mma_commit(&s.s_full[0]);
-          issue_s(1, st);
-          tc::mma_commit(&s.s_full[1]);
-          tc::mma_commit(&s.k_empty[st]);
-          if (nt == 1) tc::mma_commit(&s.q_empty);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = ((kk >> 2) * kBlockBytes + (kk & 3) * 32) >> 4;
+          if (kk == 0) tc::mma_ss_c<false>(d, a + off, b + off, id_s);
+          else tc::mma_ss_c<true>(d, a + off, b + off, id_s);
         }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      for (int i = 0; i < nt && ok; ++i) {
-        const uint32_t cur = it + i;
-        const int vst = cur % kVStages;         // V stage
-        if (lane == 0) ok = wait_or_flag(&s.v_full[vst], (cur / kVStages) & 1, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+      };
+      auto issue_pv = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t acc) {
+        tc::mma_ts(d, a, b, id_o, acc);
+#pragma unroll
+        for (int kk = 1; kk < 8; ++kk) tc::mma_ts_c<true>(d, a + kk * 8, b + kk * (2048 >> 4), id_o);
+      };
+      uint32_t kst = 0, kph = 0;     // K ring: stage and parity of the next tile to consume
+      uint32_t vst = 0, vph = 0;     // V ring
+      uint32_t tph = 0;              // parity of the current tile's S / P phases
+      bool ok = true;
+      uint32_t jc = 0;
+      for (; jw.cur.valid && ok; jw.next(), ++jc) {
+        const int nt = jw.cur.je - jw.cur.jb;
+        // The piece's last tile runs past the sequence end when L < je * 128. Its page that
+        // holds key L - 1 was loaded whole, so the V rows of the pool slots after the last key
+        // ([zl, next multiple of 16)) are zeroed, that P = 0 there cannot meet an unwritten
+        // (possibly NaN) slot; the pages after it were never loaded (zero fill).
+        const int zl = jw.cur.s.L - (jw.cur.je - 1) * kTileN;
+        const int zero_i = (zl > 0 && zl < kTileN && (zl & 15) != 0) ? nt - 1 : -1;
+        const uint32_t qph = jc & 1, oph = (jc - 1) & 1;
+        ok = wait_or_flag(&s.q_full, qph, p.status) && wait_or_flag(&s.k_full[kst], kph, p.status);
         if (!ok) break;
-        const int first_bad = pc.s.L - (pc.jb + i) * kTileN;  // V rows from here are not keys
-        if (first_bad < kTileN) {
-          // zero them so that P = 0 there cannot meet an unwritten (possibly NaN) slot
-          const int r0 = max(first_bad, 0);
-          for (int e = r0 * 16 + lane; e < kTileN * 16; e += 32) {
-            const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
-            *reinterpret_cast<uint4*>(s.v[vst][c >> 3] + r * 128 + (c & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (lane == 0) {
-          const int st1 = (cur + 1) & 1;
-          ok = wait_or_flag(&s.p_full[0], cur & 1, p.status);
-          if (ok && i == 0 && jc > 0) ok = wait_or_flag(&s.o_free[0], (jc - 1) & 1, p.status);
-          if (ok) {
-            tc::fence_after_sync();
-            issue_pv(0, vst, i > 0);
-            tc::mma_commit(&s.o_ready[0]);
-            if (i + 1 < nt) {
-              ok = wait_or_flag(&s.k_full[st1], ((cur + 1) >> 1) & 1, p.status);
-              if (ok) {
-                tc::fence_after_sync();
-                issue_s(0, st1);
-                tc::mma_commit(&s.s_full[0]);
-              }
+        tc::fence_after_sync();
+        uint64_t dk = kst ? dk1 : dk0;
+        issue_s(tmem, dq0, dk);
+        tc::mma_commit(&s.s_full[0]);
+        issue_s(tmem + 128, dq1, dk);
+        tc::mma_commit(&s.s_full[1]);
+        tc::mma_commit(&s.k_empty[kst]);
+        if (nt == 1) tc::mma_commit(&s.q_empty);
+        kph ^= kst;
+        kst ^= 1u;
+        for (int i = 0; i < nt; ++i) {
+          if (!wait_or_flag(&s.v_full[vst], vph, p.status)) { ok = false; break; }
+          if (i == zero_i) {
+            for (int e = zl * 16; e < ((zl + 15) & ~15) * 16; ++e) {
+              const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
+              *reinterpret_cast<uint4*>(s.v[vst][c >> 3] + r * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
             }
+            tc::fence_proxy_async_smem();
           }
-          if (ok) ok = wait_or_flag(&s.p_full[1], cur & 1, p.status);
-          if (ok && i == 0 && jc > 0) ok = wait_or_flag(&s.o_free[1], (jc - 1) & 1, p.status);
-          if (ok) {
+          const uint64_t dv = vst == 0 ? dv0 : (vst == 1 ? dv1 : dv2);
+          const bool more = i + 1 < nt;
+          if (!wait_or_flag(&s.p_full[0], tph, p.status) ||
+              (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[0], oph, p.status))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          issue_pv(tmem + 256, tmem, dv, i > 0 ? 1u : 0u);
+          tc::mma_commit(&s.o_ready[0]);
+          if (more) {
+            if (!wait_or_flag(&s.k_full[kst], kph, p.status)) { ok = false; break; }
             tc::fence_after_sync();
-            issue_pv(1, vst, i > 0);
-            tc::mma_commit(&s.o_ready[1]);
-            tc::mma_commit(&s.v_empty[vst]);
-            if (i + 1 < nt) {
-              issue_s(1, st1);
-              tc::mma_commit(&s.s_full[1]);
-              tc::mma_commit(&s.k_empty[st1]);
-              if (i + 2 == nt) tc::mma_commit(&s.q_empty);
-            }
+            dk = kst ? dk1 : dk0;
+            issue_s(tmem, dq0, dk);
+            tc::mma_commit(&s.s_full[0]);
           }
+          if (!wait_or_flag(&s.p_full[1], tph, p.status) ||
+              (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[1], oph, p.status))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          issue_pv(tmem + 384, tmem + 128, dv, i > 0 ? 1u : 0u);
+          tc::mma_commit(&s.o_ready[1]);
+          tc::mma_commit(&s.v_empty[vst]);
+          if (more) {
+            issue_s(tmem + 128, dq1, dk);
+            tc::mma_commit(&s.s_full[1]);
+            tc::mma_commit(&s.k_empty[kst]);
+            if (i + 2 == nt) tc::mma_commit(&s.q_empty);
+            kph ^= kst;
+            kst ^= 1u;
+          }
+          vst = vst == 2 ? 0u : vst + 1;
+          vph ^= vst == 0 ? 1u : 0u;
+          tph ^= 1u;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      it += nt;
-      ++jc;
     }
-    // every MMA this thread issued must have finished before TMEM is released
+    __syncwarp();
+    // every MMA lane 0 issued must have finished before TMEM is released
     if (lane == 0) {
       tc::mma_commit(&s.mma_done);
       wait_or_flag(&s.mma_done, 0, p.status);
@@ -679,7 +691,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         l += lsum.x + lsum.y;
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        mbar_arrive(&s.p_full[t]);
+        // one elected arrive per warp: 128 arrivals on one barrier word serialise for hundreds
+        // of cycles on the path to the next P*V
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.p_full[t]);
       }
       if (!ok) break;
       // epilogue of the piece: O / l
@@ -734,7 +749,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             empty ? -CUDART_INF_F : (m_used + log2f(l)) * kLn2;
       }
       tc::fence_before_sync();
-      mbar_arrive(&s.o_free[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.o_free[t]);
       it += nt;
     }
   }
