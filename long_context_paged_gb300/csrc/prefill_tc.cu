@@ -63,8 +63,10 @@ constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more 
 // Which of a row's 32 probability pairs per half tile take the FMA-pipe exp2 instead of the
 // MUFU unit. Measured on GB300: the MUFU unit keeps up on its own (all-MUFU was 8% faster
 // than a quarter on the FMA pipe), so none do by default.
-// L2 prefetch of the tile two ahead: off, since the round-robin schedule already keeps the
-// concurrently read K/V tiles in L2 and the extra copies cost more than they save (measured).
+// Optional L2 line prefetch of the K/V rows of the tile two ahead by the producer lanes. Off:
+// the round-robin schedule already keeps the concurrently read tiles in L2, and on GB300 it
+// measured slightly slower (as did prefetching through the TMA unit, which is busy with the
+// copies themselves).
 #ifndef PA_L2_PREFETCH
 #define PA_L2_PREFETCH 0
 #endif
@@ -111,6 +113,8 @@ struct PrefillTcParams {
   uint16_t* out;
   float* lse;
   int32_t* status;
+  const uint8_t* k_pool;  // the pools themselves (L2 prefetch addresses)
+  const uint8_t* v_pool;
   long long* ws_header;   // [0] tail units per CTA, [1] total units, [2] first tail unit,
                           // [3] jobs done whole in the round-robin phase
   long long* ws_prefix;   // [batch + 1] first unit of each sequence
@@ -407,6 +411,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     // free stage (K is needed a whole P*V earlier than V).
     const bool is_k = warp == kKProducerWarp;
     const CUtensorMap* map = is_k ? &k_map : &v_map;
+    const uint8_t* pool = is_k ? p.k_pool : p.v_pool;
     uint8_t(*ring)[2][kBlockBytes] = is_k ? s.k : s.v;
     const uint32_t nst = is_k ? 2u : static_cast<uint32_t>(kVStages);
     uint64_t* full = is_k ? s.k_full : s.v_full;
@@ -450,9 +455,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const int st = it % nst;
         const uint32_t ph = (it / nst) & 1;
         const int tok_ahead = (j + 2 < pc.je) ? page_token(j + 2) : oob_token;
-        if (PA_L2_PREFETCH && lane < kTileN / kPage && tok_ahead != oob_token) {
-          tc::tma_prefetch_3d(map, 0, pc.g, tok_ahead);
-          tc::tma_prefetch_3d(map, 64, pc.g, tok_ahead);
+        if (PA_L2_PREFETCH) {
+          // lane -> page lane / 4 of the tile two ahead, its rows 4 (lane % 4) .. + 3 (two
+          // 128-byte lines each: this KV head's 128 dims)
+          const int t = __shfl_sync(0xffffffffu, tok_ahead, lane >> 2);
+          if (t != oob_token) {
+            const uint8_t* row = pool + ((static_cast<int64_t>(t) + 4 * (lane & 3)) * kHkv + pc.g) *
+                                            (kHeadDim * 2);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              prefetch_l2(row + r * (kHkv * kHeadDim * 2));
+              prefetch_l2(row + r * (kHkv * kHeadDim * 2) + 128);
+            }
+          }
         }
         if (lane == 0) ok = wait_or_flag(&empty[st], ph ^ 1u, p.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -497,19 +512,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(s.v[0][0]), kBlockBytes, 1024);
       const uint64_t dv1 = tc::smem_desc_sw128(smem_addr(s.v[1][0]), kBlockBytes, 1024);
       const uint64_t dv2 = tc::smem_desc_sw128(smem_addr(s.v[2][0]), kBlockBytes, 1024);
-      auto issue_s = [&](uint32_t d, uint64_t a, uint64_t b) {
+      // Groups are issued in two parts so that the barrier the next group depends on can be
+      // tested (non-blocking) while the last MMAs of this group are still queued: a satisfied
+      // wait then costs no pipe time, and a blocking wait happens only when data is late.
+      auto issue_s = [&](uint32_t d, uint64_t a, uint64_t b, int k0, int k1) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
+          if (kk < k0 || kk >= k1) continue;
           const uint32_t off = ((kk >> 2) * kBlockBytes + (kk & 3) * 32) >> 4;
           if (kk == 0) tc::mma_ss_c<false>(d, a + off, b + off, id_s);
           else tc::mma_ss_c<true>(d, a + off, b + off, id_s);
         }
       };
-      auto issue_pv = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t acc) {
-        tc::mma_ts(d, a, b, id_o, acc);
+      auto issue_pv = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t acc, int k0, int k1) {
 #pragma unroll
-        for (int kk = 1; kk < 8; ++kk) tc::mma_ts_c<true>(d, a + kk * 8, b + kk * (2048 >> 4), id_o);
+        for (int kk = 0; kk < 8; ++kk) {
+          if (kk < k0 || kk >= k1) continue;
+          if (kk == 0) tc::mma_ts(d, a, b, id_o, acc);
+          else tc::mma_ts_c<true>(d, a + kk * 8, b + kk * (2048 >> 4), id_o);
+        }
       };
+      constexpr int kSplit = 6;      // MMAs of a group issued before the look-ahead test
       uint32_t kst = 0, kph = 0;     // K ring: stage and parity of the next tile to consume
       uint32_t vst = 0, vph = 0;     // V ring
       uint32_t tph = 0;              // parity of the current tile's S / P phases
@@ -528,16 +551,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         if (!ok) break;
         tc::fence_after_sync();
         uint64_t dk = kst ? dk1 : dk0;
-        issue_s(tmem, dq0, dk);
+        issue_s(tmem, dq0, dk, 0, 8);
         tc::mma_commit(&s.s_full[0]);
-        issue_s(tmem + 128, dq1, dk);
-        tc::mma_commit(&s.s_full[1]);
-        tc::mma_commit(&s.k_empty[kst]);
-        if (nt == 1) tc::mma_commit(&s.q_empty);
+        issue_s(tmem + 128, dq1, dk, 0, kSplit);
+        uint32_t kst_s1 = kst;         // K stage of the S1 group whose tail is still to issue
         kph ^= kst;
         kst ^= 1u;
         for (int i = 0; i < nt; ++i) {
-          if (!wait_or_flag(&s.v_full[vst], vph, p.status)) { ok = false; break; }
+          const bool more = i + 1 < nt;
+          bool v_ok = mbar_test(&s.v_full[vst], vph);
+          bool p0_ok = mbar_test(&s.p_full[0], tph);
+          // tail of S1 for this tile (issued at the end of the previous tile, or above)
+          issue_s(tmem + 128, dq1, dk, kSplit, 8);
+          tc::mma_commit(&s.s_full[1]);
+          tc::mma_commit(&s.k_empty[kst_s1]);
+          if (i + 1 == nt) tc::mma_commit(&s.q_empty);
+          if (!v_ok && !wait_or_flag(&s.v_full[vst], vph, p.status)) { ok = false; break; }
           if (i == zero_i) {
             for (int e = zl * 16; e < ((zl + 15) & ~15) * 16; ++e) {
               const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
@@ -547,36 +576,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             tc::fence_proxy_async_smem();
           }
           const uint64_t dv = vst == 0 ? dv0 : (vst == 1 ? dv1 : dv2);
-          const bool more = i + 1 < nt;
-          if (!wait_or_flag(&s.p_full[0], tph, p.status) ||
+          if ((!p0_ok && !wait_or_flag(&s.p_full[0], tph, p.status)) ||
               (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[0], oph, p.status))) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          issue_pv(tmem + 256, tmem, dv, i > 0 ? 1u : 0u);
+          const uint32_t acc = i > 0 ? 1u : 0u;
+          issue_pv(tmem + 256, tmem, dv, acc, 0, kSplit);
+          const bool k_ok = !more || mbar_test(&s.k_full[kst], kph);
+          issue_pv(tmem + 256, tmem, dv, acc, kSplit, 8);
           tc::mma_commit(&s.o_ready[0]);
+          bool p1_ok = false;
           if (more) {
-            if (!wait_or_flag(&s.k_full[kst], kph, p.status)) { ok = false; break; }
+            if (!k_ok && !wait_or_flag(&s.k_full[kst], kph, p.status)) { ok = false; break; }
             tc::fence_after_sync();
             dk = kst ? dk1 : dk0;
-            issue_s(tmem, dq0, dk);
+            issue_s(tmem, dq0, dk, 0, kSplit);
+            p1_ok = mbar_test(&s.p_full[1], tph);
+            issue_s(tmem, dq0, dk, kSplit, 8);
             tc::mma_commit(&s.s_full[0]);
           }
-          if (!wait_or_flag(&s.p_full[1], tph, p.status) ||
+          if ((!p1_ok && !wait_or_flag(&s.p_full[1], tph, p.status)) ||
               (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[1], oph, p.status))) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          issue_pv(tmem + 384, tmem + 128, dv, i > 0 ? 1u : 0u);
+          issue_pv(tmem + 384, tmem + 128, dv, acc, 0, 8);
           tc::mma_commit(&s.o_ready[1]);
           tc::mma_commit(&s.v_empty[vst]);
           if (more) {
-            issue_s(tmem + 128, dq1, dk);
-            tc::mma_commit(&s.s_full[1]);
-            tc::mma_commit(&s.k_empty[kst]);
-            if (i + 2 == nt) tc::mma_commit(&s.q_empty);
+            issue_s(tmem + 128, dq1, dk, 0, kSplit);
+            kst_s1 = kst;
             kph ^= kst;
             kst ^= 1u;
           }
@@ -903,6 +935,8 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.status = status;
+  p.k_pool = static_cast<const uint8_t*>(k_pool);
+  p.v_pool = static_cast<const uint8_t*>(v_pool);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_header = reinterpret_cast<long long*>(ws + w.header);
   p.ws_prefix = reinterpret_cast<long long*>(ws + w.prefix);
