@@ -378,10 +378,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
-    mbar_init(&s.q_empty, 1);
+    mbar_init(&s.q_empty, 2);       // released by each M tile's softmax (see below)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.k_full[i], 1);
-      mbar_init(&s.k_empty[i], 1);
+      mbar_init(&s.k_empty[i], 2);
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 4);   // one arrive per softmax warp
       mbar_init(&s.o_ready[i], 1);
@@ -389,7 +389,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&s.v_full[i], 1);
-      mbar_init(&s.v_empty[i], 1);
+      mbar_init(&s.v_empty[i], 2);
     }
     mbar_init(&s.mma_done, 1);
     fence_mbar_init();
@@ -512,108 +512,77 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(s.v[0][0]), kBlockBytes, 1024);
       const uint64_t dv1 = tc::smem_desc_sw128(smem_addr(s.v[1][0]), kBlockBytes, 1024);
       const uint64_t dv2 = tc::smem_desc_sw128(smem_addr(s.v[2][0]), kBlockBytes, 1024);
-      // Groups are issued in two parts so that the barrier the next group depends on can be
-      // tested (non-blocking) while the last MMAs of this group are still queued: a satisfied
-      // wait then costs no pipe time, and a blocking wait happens only when data is late.
-      auto issue_s = [&](uint32_t d, uint64_t a, uint64_t b, int k0, int k1) {
+      auto issue_s = [&](uint32_t d, uint64_t a, uint64_t b) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          if (kk < k0 || kk >= k1) continue;
           const uint32_t off = ((kk >> 2) * kBlockBytes + (kk & 3) * 32) >> 4;
           if (kk == 0) tc::mma_ss_c<false>(d, a + off, b + off, id_s);
           else tc::mma_ss_c<true>(d, a + off, b + off, id_s);
         }
       };
-      auto issue_pv = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t acc, int k0, int k1) {
+      auto issue_pv = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t acc) {
+        tc::mma_ts(d, a, b, id_o, acc);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          if (kk < k0 || kk >= k1) continue;
-          if (kk == 0) tc::mma_ts(d, a, b, id_o, acc);
-          else tc::mma_ts_c<true>(d, a + kk * 8, b + kk * (2048 >> 4), id_o);
-        }
+        for (int kk = 1; kk < 8; ++kk) tc::mma_ts_c<true>(d, a + kk * 8, b + kk * (2048 >> 4), id_o);
       };
-      constexpr int kSplit = 6;      // MMAs of a group issued before the look-ahead test
+      // This thread waits only for what it alone can know (P of each M tile, the next K tile)
+      // and commits only S completion per tile and O completion per piece: the K / V / Q stages
+      // are released by the softmax warps, which observe S_t(j) done (and through that commit
+      // also P_t V(j-1) done), and P_0(j) ready implies V(j) landed (softmax 0 checks it).
       uint32_t kst = 0, kph = 0;     // K ring: stage and parity of the next tile to consume
-      uint32_t vst = 0, vph = 0;     // V ring
+      uint32_t vst = 0;              // V ring stage of the current tile
       uint32_t tph = 0;              // parity of the current tile's S / P phases
       bool ok = true;
       uint32_t jc = 0;
       for (; jw.cur.valid && ok; jw.next(), ++jc) {
         const int nt = jw.cur.je - jw.cur.jb;
-        // The piece's last tile runs past the sequence end when L < je * 128. Its page that
-        // holds key L - 1 was loaded whole, so the V rows of the pool slots after the last key
-        // ([zl, next multiple of 16)) are zeroed, that P = 0 there cannot meet an unwritten
-        // (possibly NaN) slot; the pages after it were never loaded (zero fill).
-        const int zl = jw.cur.s.L - (jw.cur.je - 1) * kTileN;
-        const int zero_i = (zl > 0 && zl < kTileN && (zl & 15) != 0) ? nt - 1 : -1;
         const uint32_t qph = jc & 1, oph = (jc - 1) & 1;
         ok = wait_or_flag(&s.q_full, qph, p.status) && wait_or_flag(&s.k_full[kst], kph, p.status);
         if (!ok) break;
         tc::fence_after_sync();
         uint64_t dk = kst ? dk1 : dk0;
-        issue_s(tmem, dq0, dk, 0, 8);
+        issue_s(tmem, dq0, dk);
         tc::mma_commit(&s.s_full[0]);
-        issue_s(tmem + 128, dq1, dk, 0, kSplit);
-        uint32_t kst_s1 = kst;         // K stage of the S1 group whose tail is still to issue
+        issue_s(tmem + 128, dq1, dk);
+        tc::mma_commit(&s.s_full[1]);
         kph ^= kst;
         kst ^= 1u;
         for (int i = 0; i < nt; ++i) {
           const bool more = i + 1 < nt;
-          bool v_ok = mbar_test(&s.v_full[vst], vph);
-          bool p0_ok = mbar_test(&s.p_full[0], tph);
-          // tail of S1 for this tile (issued at the end of the previous tile, or above)
-          issue_s(tmem + 128, dq1, dk, kSplit, 8);
-          tc::mma_commit(&s.s_full[1]);
-          tc::mma_commit(&s.k_empty[kst_s1]);
-          if (i + 1 == nt) tc::mma_commit(&s.q_empty);
-          if (!v_ok && !wait_or_flag(&s.v_full[vst], vph, p.status)) { ok = false; break; }
-          if (i == zero_i) {
-            for (int e = zl * 16; e < ((zl + 15) & ~15) * 16; ++e) {
-              const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
-              *reinterpret_cast<uint4*>(s.v[vst][c >> 3] + r * 128 + (c & 7) * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            tc::fence_proxy_async_smem();
-          }
           const uint64_t dv = vst == 0 ? dv0 : (vst == 1 ? dv1 : dv2);
-          if ((!p0_ok && !wait_or_flag(&s.p_full[0], tph, p.status)) ||
+          const uint32_t acc = i > 0 ? 1u : 0u;
+          if (!wait_or_flag(&s.p_full[0], tph, p.status) ||
               (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[0], oph, p.status))) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t acc = i > 0 ? 1u : 0u;
-          issue_pv(tmem + 256, tmem, dv, acc, 0, kSplit);
-          const bool k_ok = !more || mbar_test(&s.k_full[kst], kph);
-          issue_pv(tmem + 256, tmem, dv, acc, kSplit, 8);
-          tc::mma_commit(&s.o_ready[0]);
-          bool p1_ok = false;
+          issue_pv(tmem + 256, tmem, dv, acc);
           if (more) {
-            if (!k_ok && !wait_or_flag(&s.k_full[kst], kph, p.status)) { ok = false; break; }
+            if (!wait_or_flag(&s.k_full[kst], kph, p.status)) { ok = false; break; }
             tc::fence_after_sync();
             dk = kst ? dk1 : dk0;
-            issue_s(tmem, dq0, dk, 0, kSplit);
-            p1_ok = mbar_test(&s.p_full[1], tph);
-            issue_s(tmem, dq0, dk, kSplit, 8);
+            issue_s(tmem, dq0, dk);
             tc::mma_commit(&s.s_full[0]);
+          } else {
+            tc::mma_commit(&s.o_ready[0]);
           }
-          if ((!p1_ok && !wait_or_flag(&s.p_full[1], tph, p.status)) ||
+          if (!wait_or_flag(&s.p_full[1], tph, p.status) ||
               (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[1], oph, p.status))) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          issue_pv(tmem + 384, tmem + 128, dv, acc, 0, 8);
-          tc::mma_commit(&s.o_ready[1]);
-          tc::mma_commit(&s.v_empty[vst]);
+          issue_pv(tmem + 384, tmem + 128, dv, acc);
           if (more) {
-            issue_s(tmem + 128, dq1, dk, 0, kSplit);
-            kst_s1 = kst;
+            issue_s(tmem + 128, dq1, dk);
+            tc::mma_commit(&s.s_full[1]);
             kph ^= kst;
             kst ^= 1u;
+          } else {
+            tc::mma_commit(&s.o_ready[1]);
           }
           vst = vst == 2 ? 0u : vst + 1;
-          vph ^= vst == 0 ? 1u : 0u;
           tph ^= 1u;
         }
       }
@@ -637,10 +606,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     const uint32_t t_o = tmem + lane_bits + 256 + t * 128;
     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
     bool ok = true;
-    uint32_t it = 0;
-    for (; jw.cur.valid && ok; jw.next()) {
+    uint32_t it = 0, jcs = 0;
+    const bool leader = quarter == 0 && lane == 0;  // releases stages for this M tile
+    for (; jw.cur.valid && ok; jw.next(), ++jcs) {
       const Piece& pc = jw.cur;
       const int nt = pc.je - pc.jb;
+      // the piece's last tile runs past the sequence end when L < je * 128: the V rows of the
+      // pool slots after the last key, [zl, next multiple of 16), are zeroed before P_0 is
+      // released (the pages after it were never loaded and arrive as zeros)
+      const int zl = pc.s.L - (pc.je - 1) * kTileN;
+      const int zero_i = (zl > 0 && zl < kTileN && (zl & 15) != 0) ? nt - 1 : -1;
       const int qrow = pc.qt * kTileM + r;
       const int qpos = pc.s.off + qrow;            // absolute position of this query
       float m_used = -CUDART_INF_F, l = 0.f;
@@ -648,6 +623,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const uint32_t cur = it + i;
         ok = __all_sync(0xffffffffu, wait_or_flag(&s.s_full[t], cur & 1, p.status));
         if (!ok) break;
+        // S_t(cur) is done, and its commit also covers P_t V(cur - 1): this M tile is finished
+        // with K stage cur and V stage cur - 1 (the last V stage of a piece is released after
+        // the epilogue's wait), and with Q after the piece's last tile
+        if (leader) {
+          mbar_arrive(&s.k_empty[cur & 1]);
+          if (i > 0) mbar_arrive(&s.v_empty[(cur - 1) % kVStages]);
+          if (i + 1 == nt) mbar_arrive(&s.q_empty);
+        }
         tc::fence_after_sync();
         uint32_t sb[128];  // raw scores (fp32 bits) of this row
 #pragma unroll
@@ -674,10 +657,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           const float m_new = grow ? mx2 : m_used;
           const float alpha = (m_used == -CUDART_INF_F) ? 0.f : fast_exp2(m_used - m_new);
           if (i > 0) {
-            // O_t holds the sum through the previous tile once its P*V has completed
-            ok = __all_sync(0xffffffffu, wait_or_flag(&s.o_ready[t], (cur - 1) & 1, p.status));
-            if (!ok) break;
-            tc::fence_after_sync();
+            // O_t holds the sum through the previous tile: P_t V(cur - 1) completed before
+            // S_t(cur), whose completion this thread has already observed
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t o32[32];
@@ -723,6 +704,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         l += lsum.x + lsum.y;
         tc::tmem_wait_st();
         tc::fence_before_sync();
+        if (t == 0 && quarter == 0) {
+          // P_0 ready also certifies V(cur): the issuer then needs no wait of its own for it
+          const uint32_t vs = cur % kVStages;
+          ok = __all_sync(0xffffffffu, wait_or_flag(&s.v_full[vs], (cur / kVStages) & 1, p.status));
+          if (!ok) break;
+          if (i == zero_i) {
+            for (int e = zl * 16 + lane; e < ((zl + 15) & ~15) * 16; e += 32) {
+              const int rr = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
+              *reinterpret_cast<uint4*>(s.v[vs][c >> 3] + rr * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            tc::fence_proxy_async_smem();
+          }
+        }
         // one elected arrive per warp: 128 arrivals on one barrier word serialise for hundreds
         // of cycles on the path to the next P*V
         __syncwarp();
@@ -730,9 +725,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       }
       if (!ok) break;
       // epilogue of the piece: O / l
-      ok = __all_sync(0xffffffffu, wait_or_flag(&s.o_ready[t], (it + nt - 1) & 1, p.status));
+      ok = __all_sync(0xffffffffu, wait_or_flag(&s.o_ready[t], jcs & 1, p.status));
       if (!ok) break;
       tc::fence_after_sync();
+      if (leader) mbar_arrive(&s.v_empty[(it + nt - 1) % kVStages]);
       const bool live = qrow < pc.s.n;
       const float inv = 1.0f / l;
       const bool whole = pc.jb == 0 && pc.je == pc.J;
