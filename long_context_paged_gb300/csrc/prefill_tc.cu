@@ -89,8 +89,11 @@ struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
   uint8_t v[kVStages][2][kBlockBytes];
   uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
+  // pv_full[st]: P_0 of the tile in V stage st is in TMEM and that V tile has landed (four
+  // softmax-0 warps arrive, the V producer arrives and its copies complete bytes on it);
+  // p1_full: P_1 of the current tile is in TMEM
+  uint64_t pv_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p1_full, o_ready[2], o_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   long long warp_sums[kThreads / 32];
@@ -383,14 +386,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 2);
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 4);   // one arrive per softmax warp
       mbar_init(&s.o_ready[i], 1);
       mbar_init(&s.o_free[i], 4);
     }
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.pv_full[i], 5);   // 4 softmax-0 warps + the V producer (+ its bytes)
       mbar_init(&s.v_empty[i], 2);
     }
+    mbar_init(&s.p1_full, 4);         // one arrive per softmax-1 warp
     mbar_init(&s.mma_done, 1);
     fence_mbar_init();
   }
@@ -414,7 +417,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     const uint8_t* pool = is_k ? p.k_pool : p.v_pool;
     uint8_t(*ring)[2][kBlockBytes] = is_k ? s.k : s.v;
     const uint32_t nst = is_k ? 2u : static_cast<uint32_t>(kVStages);
-    uint64_t* full = is_k ? s.k_full : s.v_full;
+    uint64_t* full = is_k ? s.k_full : s.pv_full;
     uint64_t* empty = is_k ? s.k_empty : s.v_empty;
     const int oob_token = static_cast<int>(p.num_pages * kPage);  // zero-filled coordinate
     bool ok = true;
@@ -525,17 +528,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
         for (int kk = 1; kk < 8; ++kk) tc::mma_ts_c<true>(d, a + kk * 8, b + kk * (2048 >> 4), id_o);
       };
-      // This thread waits only for what it alone can know (P of each M tile, the next K tile)
-      // and commits only S completion per tile and O completion per piece: the K / V / Q stages
-      // are released by the softmax warps, which observe S_t(j) done (and through that commit
-      // also P_t V(j-1) done), and P_0(j) ready implies V(j) landed (softmax 0 checks it).
+      // This thread waits only for P of each M tile (P_0's barrier also takes the V copies'
+      // bytes, so it certifies V) and for the next K tile, and commits only S completion per
+      // tile and O completion per piece: the K / V / Q stages are released by the softmax
+      // warps, which observe S_t(j) done (and through that commit also P_t V(j-1) done).
       uint32_t kst = 0, kph = 0;     // K ring: stage and parity of the next tile to consume
-      uint32_t vst = 0;              // V ring stage of the current tile
+      uint32_t vst = 0, vph = 0;     // V ring: stage and parity of the current tile
       uint32_t tph = 0;              // parity of the current tile's S / P phases
       bool ok = true;
       uint32_t jc = 0;
       for (; jw.cur.valid && ok; jw.next(), ++jc) {
         const int nt = jw.cur.je - jw.cur.jb;
+        // The piece's last tile runs past the sequence end when L < je * 128. Its page that
+        // holds key L - 1 was loaded whole, so the V rows of the pool slots after the last key
+        // ([zl, next multiple of 16)) are zeroed, that P = 0 there cannot meet an unwritten
+        // (possibly NaN) slot; the pages after it were never loaded (zero fill).
+        const int zl = jw.cur.s.L - (jw.cur.je - 1) * kTileN;
+        const int zero_i = (zl > 0 && zl < kTileN && (zl & 15) != 0) ? nt - 1 : -1;
         const uint32_t qph = jc & 1, oph = (jc - 1) & 1;
         ok = wait_or_flag(&s.q_full, qph, p.status) && wait_or_flag(&s.k_full[kst], kph, p.status);
         if (!ok) break;
@@ -551,10 +560,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           const bool more = i + 1 < nt;
           const uint64_t dv = vst == 0 ? dv0 : (vst == 1 ? dv1 : dv2);
           const uint32_t acc = i > 0 ? 1u : 0u;
-          if (!wait_or_flag(&s.p_full[0], tph, p.status) ||
+          if (!wait_or_flag(&s.pv_full[vst], vph, p.status) ||
               (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[0], oph, p.status))) {
             ok = false;
             break;
+          }
+          if (i == zero_i) {
+            for (int e = zl * 16; e < ((zl + 15) & ~15) * 16; ++e) {
+              const int r = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
+              *reinterpret_cast<uint4*>(s.v[vst][c >> 3] + r * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            tc::fence_proxy_async_smem();
           }
           tc::fence_after_sync();
           issue_pv(tmem + 256, tmem, dv, acc);
@@ -567,7 +584,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           } else {
             tc::mma_commit(&s.o_ready[0]);
           }
-          if (!wait_or_flag(&s.p_full[1], tph, p.status) ||
+          if (!wait_or_flag(&s.p1_full, tph, p.status) ||
               (i == 0 && jc > 0 && !wait_or_flag(&s.o_free[1], oph, p.status))) {
             ok = false;
             break;
@@ -583,6 +600,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             tc::mma_commit(&s.o_ready[1]);
           }
           vst = vst == 2 ? 0u : vst + 1;
+          vph ^= vst == 0 ? 1u : 0u;
           tph ^= 1u;
         }
       }
@@ -611,11 +629,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     for (; jw.cur.valid && ok; jw.next(), ++jcs) {
       const Piece& pc = jw.cur;
       const int nt = pc.je - pc.jb;
-      // the piece's last tile runs past the sequence end when L < je * 128: the V rows of the
-      // pool slots after the last key, [zl, next multiple of 16), are zeroed before P_0 is
-      // released (the pages after it were never loaded and arrive as zeros)
-      const int zl = pc.s.L - (pc.je - 1) * kTileN;
-      const int zero_i = (zl > 0 && zl < kTileN && (zl & 15) != 0) ? nt - 1 : -1;
       const int qrow = pc.qt * kTileM + r;
       const int qpos = pc.s.off + qrow;            // absolute position of this query
       float m_used = -CUDART_INF_F, l = 0.f;
@@ -704,24 +717,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         l += lsum.x + lsum.y;
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        if (t == 0 && quarter == 0) {
-          // P_0 ready also certifies V(cur): the issuer then needs no wait of its own for it
-          const uint32_t vs = cur % kVStages;
-          ok = __all_sync(0xffffffffu, wait_or_flag(&s.v_full[vs], (cur / kVStages) & 1, p.status));
-          if (!ok) break;
-          if (i == zero_i) {
-            for (int e = zl * 16 + lane; e < ((zl + 15) & ~15) * 16; e += 32) {
-              const int rr = e >> 4, c = e & 15;   // row, 16-byte chunk (8 per 64-dim block)
-              *reinterpret_cast<uint4*>(s.v[vs][c >> 3] + rr * 128 + (c & 7) * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            tc::fence_proxy_async_smem();
-          }
-        }
         // one elected arrive per warp: 128 arrivals on one barrier word serialise for hundreds
         // of cycles on the path to the next P*V
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.p_full[t]);
+        if (lane == 0) mbar_arrive(t == 0 ? &s.pv_full[cur % kVStages] : &s.p1_full);
       }
       if (!ok) break;
       // epilogue of the piece: O / l
