@@ -192,6 +192,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later); like fmaxf, a NaN
+// operand is ignored when another operand is a number.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Bring the 128-byte line holding `p` into L2 (no registers written, no completion to track).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

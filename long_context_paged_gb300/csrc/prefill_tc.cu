@@ -656,14 +656,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           for (int c = 0; c < 128; ++c)
             if (k0 + c > qpos) sb[c] = 0xff800000u;  // -inf: key after this query
         }
-        // row max over 8 independent partial maxima (no 128-long dependency chain)
+        // row max over 8 independent partial maxima (no 128-long dependency chain), two new
+        // elements per three-input max
         float pm[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(sb[k]);
+        for (int k = 0; k < 8; ++k)
+          pm[k] = fmax3(__uint_as_float(sb[k]), __uint_as_float(sb[k + 8]), __uint_as_float(sb[k + 16]));
 #pragma unroll
-        for (int c = 8; c < 128; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(sb[c]));
-        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        for (int c = 24; c < 120; c += 16) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            pm[k] = fmax3(pm[k], __uint_as_float(sb[c + k]), __uint_as_float(sb[c + 8 + k]));
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], __uint_as_float(sb[120 + k]));
+        const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                               fmaxf(pm[6], pm[7]));
         const float mx2 = mx * p.scale_log2;
         const bool grow = mx2 > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, grow)) {
