@@ -32,7 +32,8 @@
 // out-of-range coordinate and arrive as zeros; V rows of the last partial page are zeroed in
 // shared memory before use, so unwritten slots can never reach P*V.
 // The running row max moves only when a tile exceeds it by more than 8 (log2 units); O is then
-// rescaled in TMEM by its owning warps, after the previous P*V has completed.
+// rescaled in TMEM by its owning warps; the previous P*V has completed by then, since the
+// commit the warps waited on for this tile's S covers every earlier MMA of the issuer.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -73,8 +74,9 @@ constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more 
 #ifndef PA_POLY_PAIR
 #define PA_POLY_PAIR(k) false
 #endif
-// Register split: the two softmax warpgroups grow to 216 registers per thread, the
-// producer/MMA warpgroup shrinks to 72; 256 * 216 + 128 * 72 = 64,512 = 384 threads x 168, the
+// Register split: the two softmax warpgroups grow to 200 registers per thread, the
+// producer/MMA warpgroup shrinks to 104 (at 72 the issuer's loop spilled and starved the tensor
+// pipe; softmax below ~200 spills); 256 * 200 + 128 * 104 = 64,512 = 384 threads x 168, the
 // budget the CTA is launched with (checked on the host before every launch).
 constexpr int kSoftmaxRegs = 200;
 constexpr int kControlRegs = 104;
