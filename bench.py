@@ -423,7 +423,8 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="mixed_28l", choices=sorted(W.CONFIG_SEED) + ["adaptor_90min"])
+    ap.add_argument("--workload", default="mixed_28l",
+                    choices=sorted(W.CONFIG_SEED) + ["adaptor_90min", "decode_graph_buckets"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clocks-out", default=None)
@@ -446,6 +447,8 @@ def main():
     dev = f"cuda:{local}"
     if args.workload == "adaptor_90min":
         return run_adaptor(pa, args, dev, dist, world, rank)
+    if args.workload == "decode_graph_buckets":
+        return run_decode_buckets(pa, args, dev, dist, world, rank)
     step = Step(pa, args.workload, dev)
     hbm, bf16, bf16s, peak_src = peaks()
 
@@ -605,6 +608,56 @@ def run_adaptor(pa, args, dev, dist, world, rank):
                          "frac": round(tflops / bf16, 4), "peak_source": f"{peak_src} bf16_tflops",
                          "traffic": None, "algorithmic_flops_per_launch": flops},
             "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+
+
+def run_decode_buckets(pa, args, dev, dist, world, rank):
+    """Decode-step latency by batch bucket, the way a serving engine replays one CUDA graph per
+    bucket and token: 1, 2, 4, 8, 16 and 32 sequences of 1,000 cached tokens (80 s of audio
+    each; one sequence is the single-stream decode configuration). Reports microseconds per
+    replay of the decode call (split kernel + merge) and the KV read rate at each bucket."""
+    buckets = (1, 2, 4, 8, 16, 32)
+    L = 1000
+    reps = max(args.steps, 1) * 200      # each replay is microseconds long
+    lat, gbs = {}, {}
+    sampler = ClockSampler(args.clocks_out)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    for B in buckets:
+        seed = W.CONFIG_SEED["decode_b1_l1000"]
+        inp = (W.make_workload("decode_b1_l1000", device=dev) if B == 1 else
+               W.make_paged(seed + B, np.full(B, L), np.ones(B, np.int64), device=dev))
+        out = torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, W.HQ, dtype=torch.float32, device=dev)
+        ws = torch.empty(pa.decode_workspace_size(B, L), dtype=torch.uint8, device=dev)
+        call = lambda: pa.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0],
+                                            inp.block_table, inp.seq_lens, L, inp.scale,
+                                            out=out, lse=lse, workspace=ws)
+        call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        (t,) = max_over_ranks(dist, [timed_replays(g, reps, max(args.warmup, 0) * 20, dist)], dev)
+        lat[str(B)] = round(t / reps * 1e6, 2)
+        gbs[str(B)] = round(B * L * W.kv_bytes_per_token() / (t / reps) / 1e9, 1)
+        del g
+    clocks = sampler.stop(device_uuid()) if rank == 0 else None
+    hbm, bf16, bf16s, peak_src = peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "decode step latency by batch bucket (CUDA-graph replay), us", "value": lat["1"],
+            "unit": "us", "n_gpus": world, "steps": reps, "warmup": max(args.warmup, 0) * 20,
+            "ms_per_step": round(lat["1"] / 1e3, 5), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode_graph_buckets", "seq_len": L, "buckets": list(buckets),
+                       "timing": "CUDA events around back-to-back replays of one graph per bucket"},
+            "latency_us": lat, "kv_read_gbs": gbs,
+            "roofline": {"kernel": "attn_decode_paged (decode_splitkv + merge)", "bound": "hbm",
+                         "achieved": gbs["32"], "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs["32"] / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
+                         "traffic": None, "note": "at the 32-sequence bucket; small buckets are latency-bound"},
+            "gpu_launches": 2 * reps * len(buckets), "clocks": clocks}), flush=True)
 
 
 def run_reference(args, world, rank):

@@ -22,6 +22,7 @@
 //  * fp32 math on bf16 loads, paired fp32 FMAs (fma.rn.f32x2). The running max is only moved
 //    when a page exceeds it by more than 8 (log2 units), so the accumulators are rescaled
 //    rarely; probabilities stay <= 2^8 and the result is exact up to rounding.
+#include <algorithm>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -39,7 +40,10 @@ constexpr int kStages = 3;
 constexpr uint32_t kPageBytes = kPage * kHkv * kHeadDim * 2;  // K (or V) of one page
 constexpr int kMaxBatch = 4096;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kMinPagesPerCta = 4;
+#ifndef PA_DECODE_MIN_PAGES
+#define PA_DECODE_MIN_PAGES 1
+#endif
+constexpr int kMinPagesPerCta = PA_DECODE_MIN_PAGES;
 
 struct DecodeSmem {
   uint8_t kv[kStages][2][kPageBytes];
@@ -146,8 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
   build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
 
   const int total = s.total;
-  // pages per CTA: an equal share, but at least kMinPagesPerCta so that short batches are not
-  // cut into one-page pieces whose partials would then all need merging
+  // pages per CTA: an equal share (at least kMinPagesPerCta). A short batch is spread over as
+  // many SMs as it has pages: one SM ingests a 32 KB page in well under a microsecond, so a
+  // single-sequence decode is latency-bound, and its partials merge in parallel per head.
   const int W = max((total + gridDim.x - 1) / gridDim.x, kMinPagesPerCta);
   if (blockIdx.x == 0) {
     if (tid == 0) {
@@ -401,47 +406,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
 }
 
 // Merge the partial results of sequences that crossed a CTA range boundary; also writes the
-// result of empty sequences (o = 0, lse = -inf). One CTA per sequence, one warp per head.
+// result of empty sequences (o = 0, lse = -inf). One 4-warp CTA per (sequence, head): each warp
+// takes every fourth partial (a lane holds 4 of the 128 dims), with several partials' loads in
+// flight, and the warps combine through shared memory, so a single long sequence cut into many
+// partials is merged by 16 SMs without a long chain of dependent loads.
 // Launched as a programmatic dependent of decode_splitkv_kernel: its CTAs may start while the
 // split kernel is still running and wait (griddepcontrol.wait) until that grid has completed
 // and its writes are visible, which hides this launch behind the split kernel.
-__global__ void __launch_bounds__(kHq * 32) decode_merge_kernel(const DecodeParams p) {
+constexpr int kMergeWarps = 4;
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.x;
-  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float red_m[kMergeWarps], red_w[kMergeWarps];
+  __shared__ float4 red_o[kMergeWarps][32];
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p0 = p.ws_prefix[b], p1 = p.ws_prefix[b + 1];
   uint16_t* orow = p.out + (static_cast<int64_t>(b) * kHq + h) * kHeadDim + 4 * lane;
   if (p1 == p0) {
-    *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
-    if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = -CUDART_INF_F;
+    if (warp == 0) {
+      *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+      if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = -CUDART_INF_F;
+    }
     return;
   }
   const int W = p.ws_header[0];
   const int c0 = p0 / W, c1 = (p1 - 1) / W;
   if (c0 == c1) return;  // finished inside one CTA
+  // max of the partial LSEs
   float m = -CUDART_INF_F;
-  for (int c = c0 + lane; c <= c1; c += 32) m = fmaxf(m, p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h]);
+  for (int c = c0 + threadIdx.x; c <= c1; c += kMergeWarps * 32)
+    m = fmaxf(m, p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red_m[warp] = m;
+  __syncthreads();
+  m = red_m[0];
+#pragma unroll
+  for (int k = 1; k < kMergeWarps; ++k) m = fmaxf(m, red_m[k]);
+  // this warp's partials: c0 + warp, c0 + warp + 4, ...
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  for (int base = c0; base <= c1; base += 32) {
-    // lane k owns the weight of part base + k; every lane then loads its 4 dims of each part
-    const int c = base + lane;
-    const float w = c <= c1
-        ? fast_exp2((p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h] - m) * kLog2e) : 0.f;
+  const float* src = p.ws_o + (static_cast<int64_t>(b) * kHq + h) * kHeadDim + 4 * lane;
+#pragma unroll 4
+  for (int c = c0 + warp; c <= c1; c += kMergeWarps) {
+    const float w = fast_exp2((p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h] - m) * kLog2e);
+    const float4 o = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(c) * kHq * kHeadDim);
     wsum += w;
-    const int n = min(32, c1 - base + 1);
-    const float* src = p.ws_o + ((static_cast<int64_t>(b) + base) * kHq + h) * kHeadDim + 4 * lane;
-#pragma unroll 8
-    for (int k = 0; k < n; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      const float4 o = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(k) * kHq * kHeadDim);
-      acc.x += wk * o.x; acc.y += wk * o.y; acc.z += wk * o.z; acc.w += wk * o.w;
-    }
+    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
   }
+  red_o[warp][lane] = acc;
+  if (lane == 0) red_w[warp] = wsum;
+  __syncthreads();
+  if (warp != 0) return;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  for (int k = 1; k < kMergeWarps; ++k) {
+    const float4 o = red_o[k][lane];
+    acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+    wsum += red_w[k];
+  }
   const float inv = 1.0f / wsum;
   *reinterpret_cast<uint2*>(orow) =
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
@@ -504,10 +526,15 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
        reinterpret_cast<uintptr_t>(v_pool) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return PA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
-  const int grid = decode_grid_size();
-  if (grid <= 0) return PA_ERR_CUDA;
+  const int sm_grid = decode_grid_size();
+  if (sm_grid <= 0) return PA_ERR_CUDA;
+  if (workspace_bytes < ws_layout(batch, sm_grid).total) return PA_ERR_WORKSPACE_TOO_SMALL;
+  // one CTA per SM, but no more CTAs than the batch can have pages (a short batch then
+  // launches only the CTAs that get work)
+  const int64_t page_bound =
+      static_cast<int64_t>(batch) * ((static_cast<int64_t>(max_seq_len) + kPage - 1) / kPage);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sm_grid, page_bound)));
   const WsLayout w = ws_layout(batch, grid);
-  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   static thread_local int configured_device = -1;
   int dev = 0;
@@ -517,6 +544,11 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sizeof(DecodeSmem)));
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(decode)");
+    // the merge kernel uses no shared memory; giving it the split kernel's carveout keeps the
+    // SMs from reconfiguring shared memory / L1 between the two launches of every call
+    e = cudaFuncSetAttribute(decode_merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(decode merge)");
     configured_device = dev;
   }
 
@@ -545,8 +577,8 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   PA_CHECK_LAUNCH("decode_splitkv_kernel");
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(batch);
-    cfg.blockDim = dim3(kHq * 32);
+    cfg.gridDim = dim3(batch, kHq);
+    cfg.blockDim = dim3(kMergeWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

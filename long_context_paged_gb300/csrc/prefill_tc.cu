@@ -917,6 +917,10 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(prefill_tc)");
+    // same carveout for the shared-memory-free merge kernel: no reconfiguration between them
+    e = cudaFuncSetAttribute(prefill_merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(prefill merge)");
     // The in-kernel register split needs the full launch budget; a build that launched with
     // fewer registers per thread would make setmaxnreg.inc wait forever, so refuse to launch.
     cudaFuncAttributes fa;
