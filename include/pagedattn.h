@@ -215,6 +215,8 @@ pa_status attn_merge_lse(int32_t num_parts, int32_t rows, int32_t heads, int32_t
  *   out      bf16 [T][1024]
  *   workspace    at least pa_adaptor_workspace_size(num_frames) bytes (the bf16 hidden
  *                activations, [T][1024]); 16-byte aligned.
+ * frames, w1, w2, gamma, beta, out and workspace must be 16-byte aligned, else
+ * PA_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------------------------ */
 size_t pa_adaptor_workspace_size(int32_t num_frames);
 

@@ -165,11 +165,15 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
         uint32_t v[32];
         tc::tmem_ld32(tmem + lane_bits + acc * kBN + c * 32, v);
         tc::tmem_wait_ld();
+        // the chunk's 32 biases: one coalesced load, then broadcast lane by lane
+        const float bias_lane = __ldg(p.bias + n0 + c * 32 + lane);
         float f[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float x = __uint_as_float(v[i]) + __ldg(p.bias + n0 + c * 32 + i);
-          if (p.silu) x = x / (1.0f + __expf(-x));
+          float x = __uint_as_float(v[i]) + __shfl_sync(0xffffffffu, bias_lane, i);
+          // SiLU x * sigmoid(x) with the fast reciprocal division (the result is rounded to
+          // bf16; exact for x -> -inf: 1 + e^-x overflows to inf and x / inf -> -0)
+          if (p.silu) x = __fdividef(x, 1.0f + __expf(-x));
           f[i] = x;
         }
         if (row < p.M) {
@@ -232,9 +236,16 @@ __global__ void __launch_bounds__(256) layernorm_rows_kernel(uint16_t* y, int32_
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int col = 8 * (lane + 32 * i);
+    // the scale and shift of these 8 columns as two 16-byte loads each
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma + col));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma + col + 4));
+    const float4 b0 = __ldg(reinterpret_cast<const float4*>(beta + col));
+    const float4 b1 = __ldg(reinterpret_cast<const float4*>(beta + col + 4));
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
     float o[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) o[k] = (v[8 * i + k] - mean) * rstd * gamma[col + k] + beta[col + k];
+    for (int k = 0; k < 8; ++k) o[k] = (v[8 * i + k] - mean) * rstd * g[k] + bb[k];
     uint4 w;
     w.x = pack_bf16x2(o[0], o[1]);
     w.y = pack_bf16x2(o[2], o[3]);
@@ -294,7 +305,8 @@ extern "C" pa_status adaptor_mlp_merge4(int32_t num_frames, const void* frames, 
     return PA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(frames) | reinterpret_cast<uintptr_t>(w1) |
        reinterpret_cast<uintptr_t>(w2) | reinterpret_cast<uintptr_t>(out) |
-       reinterpret_cast<uintptr_t>(workspace)) & 15u)
+       reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(gamma) |
+       reinterpret_cast<uintptr_t>(beta)) & 15u)
     return PA_ERR_INVALID_ARG;
   if (workspace_bytes < pa_adaptor_workspace_size(num_frames)) return PA_ERR_WORKSPACE_TOO_SMALL;
   const int T = num_frames / kMerge;
