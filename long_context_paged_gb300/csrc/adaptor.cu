@@ -13,6 +13,11 @@
 // through a 4-stage TMA ring (A 16 KB + B 32 KB per stage, 128-byte swizzle), fp32
 // accumulators in two 256-column TMEM buffers so the epilogue of one tile overlaps the MMAs of
 // the next. Warps: 0-3 epilogue (bias, SiLU, bf16, store), 4 TMA producer, 5 MMA issuer.
+// At K = 4096 a tile pulls 3 MB through L2, which bounds the main loop, so CTAs run in
+// clusters of two on row tiles 2i, 2i + 1 of the same column tile: each loads its own A and
+// half of the shared B tile, multicast into both CTAs' shared memory (2 MB per tile instead of
+// 3); a stage is refilled once both CTAs' MMAs have released it (their commits arrive on both
+// CTAs' barriers).
 // LayerNorm is a row-wise pass (one warp per row) over the staged pre-norm rows.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -42,6 +47,10 @@ constexpr int kGemmThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KB
 
+constexpr int kCluster = 2;                  // CTAs sharing a B tile
+constexpr uint16_t kClusterMask = 0x3;
+constexpr uint32_t kBHalfBytes = kBBytes / kCluster;
+
 struct GemmSmem {  // placed at a 1024-byte aligned address
   uint8_t a[kStages][kABytes];
   uint8_t b[kStages][kBBytes];
@@ -60,6 +69,39 @@ struct GemmParams {
   int32_t* status;
 };
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Both CTAs of the cluster: barrier over every thread (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Tiled 2-D TMA load whose data and byte count land at the same shared-memory offsets (buffer
+// and mbarrier) in every CTA of `mask` within this cluster.
+__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map,
+                                                      int c0, int c1, uint64_t* bar,
+                                                      uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+
+// Arrive (once) on the mbarrier at `bar`'s offset in every CTA of `mask` when all tcgen05
+// operations this thread issued so far have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int32_t* status) {
   if (mbar_wait_bounded(bar, parity)) return true;
   flag_error(status, PA_DEV_ERR_TIMEOUT);
@@ -74,14 +116,17 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
   GemmSmem& s = *reinterpret_cast<GemmSmem*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (p.M + kBM - 1) / kBM, n_tiles = p.N / kBN;
-  const int tiles = m_tiles * n_tiles;
+  // a unit is a pair of row tiles (2i, 2i + 1) x one column tile; this CTA takes row tile
+  // 2i + rank (past the last row tile it loads zeros and stores nothing)
+  const int units = ((m_tiles + 1) / 2) * n_tiles;
   const int k_blocks = p.K / kBK;
-  if (static_cast<int>(blockIdx.x) >= tiles) return;
+  const int rank = static_cast<int>(cluster_rank());
+  const int cl = static_cast<int>(blockIdx.x) / kCluster, n_cl = static_cast<int>(gridDim.x) / kCluster;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1);
+      mbar_init(&s.empty[i], kCluster);   // one commit from each CTA's MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.acc_full[i], 1);
@@ -92,7 +137,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
   }
   if (warp == 5) tc::tmem_alloc<512>(&s.tmem_base);
   tc::fence_before_sync();
-  __syncthreads();
+  cluster_sync();   // the peer's barriers exist before anything is multicast into them
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
 
@@ -101,15 +146,17 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
+      for (int u = cl; u < units && ok; u += n_cl) {
+        const int m0 = (2 * (u / n_tiles) + rank) * kBM, n0 = (u % n_tiles) * kBN;
         for (int kb = 0; kb < k_blocks && ok; ++kb, ++it) {
           const int st = it % kStages;
+          // both CTAs' MMAs have released this stage, so both may now receive data
           ok = wait_or_flag(&s.empty[st], ((it / kStages) & 1) ^ 1u, p.status);
           if (!ok) break;
           mbar_arrive_expect_tx(&s.full[st], kABytes + kBBytes);
           tc::tma_load_2d(s.a[st], &a_map, kb * kBK, m0, &s.full[st]);
-          tc::tma_load_2d(s.b[st], &b_map, kb * kBK, n0, &s.full[st]);
+          tma_load_2d_multicast(s.b[st] + rank * kBHalfBytes, &b_map, kb * kBK,
+                                n0 + rank * (kBN / kCluster), &s.full[st], kClusterMask);
         }
       }
       // do not leave while copies into shared memory may still be landing
@@ -123,7 +170,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
       constexpr uint32_t idesc = tc::idesc_bf16(kBM, kBN, 0, 0);
       uint32_t it = 0, tc_n = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc_n) {
+      for (int u = cl; u < units && ok; u += n_cl, ++tc_n) {
         const uint32_t acc = tc_n & 1;
         ok = wait_or_flag(&s.acc_empty[acc], ((tc_n >> 1) & 1) ^ 1u, p.status);
         if (!ok) break;
@@ -139,7 +186,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
             tc::mma_ss(tmem + acc * kBN, tc::smem_desc_sw128(aa + kk * 32, 16, 1024),
                        tc::smem_desc_sw128(bb + kk * 32, 16, 1024), idesc,
                        (kb > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(&s.empty[st]);
+          mma_commit_multicast(&s.empty[st], kClusterMask);
         }
         if (ok) tc::mma_commit(&s.acc_full[acc]);
       }
@@ -152,12 +199,12 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
     const int r = warp * 32 + lane;  // row of the tile = TMEM lane
     const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t tc_n = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tc_n) {
+    for (int u = cl; u < units; u += n_cl, ++tc_n) {
       const uint32_t acc = tc_n & 1;
       if (!__all_sync(0xffffffffu, wait_or_flag(&s.acc_full[acc], (tc_n >> 1) & 1, p.status)))
         break;
       tc::fence_after_sync();
-      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
+      const int m0 = (2 * (u / n_tiles) + rank) * kBM, n0 = (u % n_tiles) * kBN;
       const int row = m0 + r;
       uint16_t* dst = p.c + static_cast<int64_t>(row) * p.N + n0;
 #pragma unroll 1
@@ -195,7 +242,8 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
   }
 
   tc::fence_before_sync();
-  __syncthreads();
+  // the peer may still multicast into this CTA or arrive on its barriers until it is done too
+  cluster_sync();
   if (warp == 5) {
     tc::fence_after_sync();
     tc::tmem_dealloc<512>(tmem);
@@ -262,7 +310,7 @@ pa_status launch_gemm(const void* a, int64_t lda_bytes, const void* b, int M, in
   if (!make_map_2d(&am, a, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
                    static_cast<uint64_t>(lda_bytes), kBM) ||
       !make_map_2d(&bm, b, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                   static_cast<uint64_t>(K) * 2, kBN)) {
+                   static_cast<uint64_t>(K) * 2, kBN / kCluster)) {
     snprintf_error("cuTensorMapEncodeTiled failed for the adaptor operands");
     return PA_ERR_CUDA;
   }
@@ -276,11 +324,23 @@ pa_status launch_gemm(const void* a, int64_t lda_bytes, const void* b, int M, in
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(gemm)");
     configured_device = dev;
   }
-  const int grid = sm_count_current_device();
-  if (grid <= 0) return PA_ERR_CUDA;
+  const int sms = sm_count_current_device();
+  if (sms < kCluster) return PA_ERR_CUDA;
   GemmParams p{M, N, K, bias, static_cast<uint16_t*>(c), silu ? 1 : 0, status};
-  gemm_bias_act_kernel<<<grid, kGemmThreads, smem, stream>>>(am, bm, p);
-  PA_CHECK_LAUNCH("gemm_bias_act_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms / kCluster * kCluster);   // one CTA per SM, in pairs
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bias_act_kernel, am, bm, p);
+  if (e != cudaSuccess) return record_cuda_error(e, "gemm_bias_act_kernel");
   return PA_OK;
 }
 
