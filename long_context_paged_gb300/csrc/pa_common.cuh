@@ -90,27 +90,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return d;
 }
 
-// 2^x of two values on the FMA pipe, leaving the MUFU unit to other elements. x = n + f with
-// n = round(x) taken from the low mantissa bits of x + 1.5*2^23 and f in [-1/2, 1/2]; 2^f is a
-// cubic fitted to 2^f on [-1/2, 1/2] by iteratively reweighted least squares in relative error
-// (max relative error 7.5e-5 in fp32 Horner form, far below the bf16 rounding of P); 2^n is
-// added to the exponent field. Inputs below -126 are clamped (the result is then below 2^-125,
-// i.e. zero for every later use).
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -126.0f);
-  x.y = fmaxf(x.y, -126.0f);
-  const float2 t = add2(x, make_float2(kMagic, kMagic));
-  const float2 r = add2(t, make_float2(-kMagic, -kMagic));
-  const float2 f = add2(x, make_float2(-r.x, -r.y));
-  float2 q = fma2(make_float2(0.0551716685f, 0.0551716685f), f,
-                  make_float2(0.2426111400f, 0.2426111400f));
-  q = fma2(q, f, make_float2(0.6932609677f, 0.6932609677f));
-  q = fma2(q, f, make_float2(0.9999280572f, 0.9999280572f));
-  return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
-}
-
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -158,20 +137,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of the same condition (no suspension): lets a thread look ahead at a
-// barrier while earlier asynchronous work is still in flight.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -198,11 +163,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
-}
-
-// Bring the 128-byte line holding `p` into L2 (no registers written, no completion to track).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Bulk global->shared copy completing on an mbarrier (bytes: multiple of 16, both addresses

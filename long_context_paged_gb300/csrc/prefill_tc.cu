@@ -61,19 +61,6 @@ constexpr uint32_t kTileBytes = 2 * kBlockBytes;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxBatch = 128;   // chunks per call (the unit prefix lives in shared memory)
 constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more stage in flight
-// Which of a row's 32 probability pairs per half tile take the FMA-pipe exp2 instead of the
-// MUFU unit. Measured on GB300: the MUFU unit keeps up on its own (all-MUFU was 8% faster
-// than a quarter on the FMA pipe), so none do by default.
-// Optional L2 line prefetch of the K/V rows of the tile two ahead by the producer lanes. Off:
-// the round-robin schedule already keeps the concurrently read tiles in L2, and on GB300 it
-// measured slightly slower (as did prefetching through the TMA unit, which is busy with the
-// copies themselves).
-#ifndef PA_L2_PREFETCH
-#define PA_L2_PREFETCH 0
-#endif
-#ifndef PA_POLY_PAIR
-#define PA_POLY_PAIR(k) false
-#endif
 // Register split: the two softmax warpgroups grow to 200 registers per thread, the
 // producer/MMA warpgroup shrinks to 104 (at 72 the issuer's loop spilled and starved the tensor
 // pipe; softmax below ~200 spills); 256 * 200 + 128 * 104 = 64,512 = 384 threads x 168, the
@@ -118,8 +105,6 @@ struct PrefillTcParams {
   uint16_t* out;
   float* lse;
   int32_t* status;
-  const uint8_t* k_pool;  // the pools themselves (L2 prefetch addresses)
-  const uint8_t* v_pool;
   long long* ws_header;   // [0] tail units per CTA, [1] total units, [2] first tail unit,
                           // [3] jobs done whole in the round-robin phase
   long long* ws_prefix;   // [batch + 1] first unit of each sequence
@@ -416,7 +401,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     // free stage (K is needed a whole P*V earlier than V).
     const bool is_k = warp == kKProducerWarp;
     const CUtensorMap* map = is_k ? &k_map : &v_map;
-    const uint8_t* pool = is_k ? p.k_pool : p.v_pool;
     uint8_t(*ring)[2][kBlockBytes] = is_k ? s.k : s.v;
     const uint32_t nst = is_k ? 2u : static_cast<uint32_t>(kVStages);
     uint64_t* full = is_k ? s.k_full : s.pv_full;
@@ -460,20 +444,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const int st = it % nst;
         const uint32_t ph = (it / nst) & 1;
         const int tok_ahead = (j + 2 < pc.je) ? page_token(j + 2) : oob_token;
-        if (PA_L2_PREFETCH) {
-          // lane -> page lane / 4 of the tile two ahead, its rows 4 (lane % 4) .. + 3 (two
-          // 128-byte lines each: this KV head's 128 dims)
-          const int t = __shfl_sync(0xffffffffu, tok_ahead, lane >> 2);
-          if (t != oob_token) {
-            const uint8_t* row = pool + ((static_cast<int64_t>(t) + 4 * (lane & 3)) * kHkv + pc.g) *
-                                            (kHeadDim * 2);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              prefetch_l2(row + r * (kHkv * kHeadDim * 2));
-              prefetch_l2(row + r * (kHkv * kHeadDim * 2) + 128);
-            }
-          }
-        }
         if (lane == 0) ok = wait_or_flag(&empty[st], ph ^ 1u, p.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -711,13 +681,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           for (int k = 0; k < 32; ++k) {
             const float2 x = fma2(make_float2(__uint_as_float(sb[c * 64 + 2 * k]),
                                               __uint_as_float(sb[c * 64 + 2 * k + 1])), sc2, nm2);
-            float2 e;
-            if (PA_POLY_PAIR(k)) {
-              e = exp2_poly2(x);
-            } else {
-              e.x = fast_exp2(x.x);
-              e.y = fast_exp2(x.y);
-            }
+            // exp2 on the MUFU unit (moving a share of them to an FMA-pipe polynomial, or
+            // fusing the row max into this pass, measured slower on GB300)
+            const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
             ls[k & 3] = add2(ls[k & 3], e);
             pk[k] = pack_bf16x2(e.x, e.y);
           }
@@ -944,8 +910,6 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.status = status;
-  p.k_pool = static_cast<const uint8_t*>(k_pool);
-  p.v_pool = static_cast<const uint8_t*>(v_pool);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_header = reinterpret_cast<long long*>(ws + w.header);
   p.ws_prefix = reinterpret_cast<long long*>(ws + w.prefix);
