@@ -424,7 +424,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="mixed_28l",
-                    choices=sorted(W.CONFIG_SEED) + ["adaptor_90min", "decode_graph_buckets"])
+                    choices=sorted(W.CONFIG_SEED) + ["adaptor_90min", "decode_graph_buckets",
+                                                     "prefill_ragged_mix"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clocks-out", default=None)
@@ -449,6 +450,8 @@ def main():
         return run_adaptor(pa, args, dev, dist, world, rank)
     if args.workload == "decode_graph_buckets":
         return run_decode_buckets(pa, args, dev, dist, world, rank)
+    if args.workload == "prefill_ragged_mix":
+        return run_prefill_ragged(pa, args, dev, dist, world, rank)
     step = Step(pa, args.workload, dev)
     hbm, bf16, bf16s, peak_src = peaks()
 
@@ -608,6 +611,51 @@ def run_adaptor(pa, args, dev, dist, world, rank):
                          "frac": round(tflops / bf16, 4), "peak_source": f"{peak_src} bf16_tflops",
                          "traffic": None, "algorithmic_flops_per_launch": flops},
             "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+
+
+def run_prefill_ragged(pa, args, dev, dist, world, rank):
+    """Several requests' prompt chunks coalesced into one attn_prefill_chunk call: chunks of
+    4,096 / 2,048 / 1,024 / 512 queries at offsets 28,672 / 61,440 / 10,000 / 0 (a new request),
+    plus a 1-token and a 2-token extend, as a scheduler packs a prefill step."""
+    inp = W.make_ragged_prefill(device=dev)
+    q_lens, seq_lens = inp.host_q_lens, inp.host_seq_lens
+    rows = int(q_lens.sum())
+    max_s = int(seq_lens.max())
+    out = torch.empty(rows, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(rows, W.HQ, dtype=torch.float32, device=dev)
+    ws = torch.empty(pa.prefill_workspace_size(len(q_lens), int(q_lens.max()), max_s),
+                     dtype=torch.uint8, device=dev)
+    call = lambda: pa.attn_prefill_chunk(inp.q[0], inp.cu_q_lens, inp.k_pools[0], inp.v_pools[0],
+                                         inp.block_table, inp.seq_lens, int(q_lens.max()), max_s,
+                                         inp.scale, out=out, lse=lse, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    sampler = ClockSampler(args.clocks_out)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    (t,) = max_over_ranks(dist, [timed_replays(g, args.steps, max(args.warmup, 0), dist)], dev)
+    clocks = sampler.stop(device_uuid()) if rank == 0 else None
+    flops = prefill_flops(sum(prefill_pairs(int(L), int(q)) for L, q in zip(seq_lens, q_lens)))
+    tflops = weak_scaling_rate(flops * args.steps, world, t) / 1e12
+    hbm, bf16, bf16s, peak_src = peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "paged GQA attn: prefill-chunk TFLOP/s, ragged multi-request call",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t * 1e3 / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K/V, paged 16, scattered pages)",
+            "config": {"workload": "prefill_ragged_mix", "chunks": [list(x) for x in W.RAGGED_PREFILL_MIX],
+                       "query_rows": rows, "timing": "CUDA events around CUDA-graph replays of the call"},
+            "roofline": {"kernel": "attn_prefill_chunk", "bound": "tensor", "achieved": round(tflops, 2),
+                         "peak": bf16, "unit": "TFLOP/s", "frac": round(tflops / bf16, 4),
+                         "peak_source": f"{peak_src} bf16_tflops", "traffic": None,
+                         "algorithmic_flops_per_launch": flops},
+            "gpu_launches": 2 * args.steps, "clocks": clocks}), flush=True)
 
 
 def run_decode_buckets(pa, args, dev, dist, world, rank):

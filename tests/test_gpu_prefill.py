@@ -76,6 +76,23 @@ def test_prefill_full_size_last_chunk(cuda_lib):
     assert cuda_lib.read_device_status(status) == 0
 
 
+def test_prefill_ragged_mix_full_size(cuda_lib):
+    """The bench's coalesced step: chunks of 4,096 / 2,048 / 1,024 / 512 queries at offsets
+    28,672 / 61,440 / 10,000 / 0 and 1- and 2-token extends in one call; sampled rows of every
+    chunk (its first and last 16, page and tile edges, random) and both extends in full."""
+    inp = W.make_ragged_prefill(device="cuda", poison=True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefill(cuda_lib, inp, status=status)
+    cu = host(inp.cu_q_lens)
+    rows = []
+    for b in range(len(cu) - 1):
+        n = int(cu[b + 1] - cu[b])
+        rows += [int(cu[b]) + r for r in (sampled_rows(n, 10 + b, count=24) if n > 40 else range(n))]
+    ref_o, ref_l = oracle_prefill(inp, rows=rows)
+    check_attn(out, lse, ref_o, ref_l, rows=rows, what="ragged prefill mix")
+    assert cuda_lib.read_device_status(status) == 0
+
+
 def test_prefill_chunk_longer_than_sequence_is_flagged(cuda_lib):
     inp = W.make_paged(202, [50], [20], device="cuda")
     sl = inp.seq_lens.clone()

@@ -223,6 +223,20 @@ def make_workload(name: str, *, device="cpu", poison=False, seed=None, **kw) -> 
     return make_paged(seed, L, ql, poison=poison, device=device, **kw)
 
 
+# Coalesced prefill step of several requests (q_len, offset): prompt chunks at different depths,
+# a new request's first chunk (offset 0), and 1- and 2-token extends.
+RAGGED_PREFILL_MIX = ((4096, 28_672), (2048, 61_440), (1024, 10_000), (512, 0), (1, 5_000),
+                      (2, 20_000))
+RAGGED_PREFILL_SEED = 1007
+
+
+def make_ragged_prefill(*, device="cpu", poison=False) -> "PagedInputs":
+    """The RAGGED_PREFILL_MIX batch: one sequence per request, its chunk's keys included."""
+    q_lens = [q for q, _ in RAGGED_PREFILL_MIX]
+    seq_lens = [q + o for q, o in RAGGED_PREFILL_MIX]
+    return make_paged(RAGGED_PREFILL_SEED, seq_lens, q_lens, poison=poison, device=device)
+
+
 def kv_bytes_per_token(num_kv_heads: int = HKV, head_dim: int = HEAD_DIM) -> int:
     """K plus V bytes of one token in one layer (bf16)."""
     return 2 * num_kv_heads * head_dim * 2
