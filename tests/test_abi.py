@@ -75,3 +75,28 @@ def test_argument_errors_are_rejected_before_launch(lib):
                                  null, null, null, 0, null, null) == 0
     assert lib.attn_merge_lse(1, 0, 16, 128, null, null, null, null, null) == 0
     assert lib.pa_read_device_status(null, null, null) == 1
+
+
+def test_adaptor_argument_errors_are_rejected_before_launch(lib):
+    """adaptor_mlp_merge4 validates everything on the host; the fake pointers below are never
+    dereferenced because every case returns before anything is launched."""
+    vp, fp = ctypes.c_void_p, ctypes.c_void_p
+    A = 1 << 12                      # a 16-byte aligned fake address
+    ok = [vp(A), vp(A), fp(A), vp(A), fp(A), fp(A), fp(A)]   # frames, w1, b1, w2, b2, gamma, beta
+
+    def call(num_frames, ptrs=ok, eps=1e-5, out=vp(A), ws=vp(A), ws_bytes=1 << 30):
+        return lib.adaptor_mlp_merge4(num_frames, *ptrs, ctypes.c_float(eps), out, ws,
+                                      ctypes.c_size_t(ws_bytes), None, None)
+
+    assert call(6) == 1                                  # not a multiple of the 4x merge
+    assert call(-4) == 1
+    assert call(8, eps=-1.0) == 1
+    assert call(0) == 0                                  # empty work is a no-op success
+    assert call(8, ptrs=[None] + ok[1:]) == 1            # null input
+    misaligned_gamma = ok[:5] + [fp(A + 4)] + ok[6:]
+    assert call(8, ptrs=misaligned_gamma) == 1           # gamma / beta are read as 16-byte vectors
+    assert call(8, out=vp(A + 8)) == 1
+    need = lib.pa_adaptor_workspace_size(8)
+    assert need == 2 * 1024 * 2 + 256                    # bf16 hidden rows of the 2 merged tokens
+    assert call(8, ws_bytes=need - 1) == 3               # workspace too small
+    assert lib.pa_adaptor_workspace_size(-1) == 0
