@@ -406,18 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
 }
 
 // Merge the partial results of sequences that crossed a CTA range boundary; also writes the
-// result of empty sequences (o = 0, lse = -inf). One 4-warp CTA per (sequence, head): each warp
-// takes every fourth partial (a lane holds 4 of the 128 dims), with several partials' loads in
-// flight, and the warps combine through shared memory, so a single long sequence cut into many
-// partials is merged by 16 SMs without a long chain of dependent loads.
+// result of empty sequences (o = 0, lse = -inf). One CTA per (sequence, head) of kWarps warps:
+// each warp takes every kWarps-th partial (a lane holds 4 of the 128 dims) in one online pass
+// with its own running maximum, four partials' loads in flight at a time, and the warps combine
+// through shared memory. When sequences are cut into more partials than 4 warps take in one round
+// (few sequences over many CTAs), 16 warps are used, so that a sequence split over ~64 CTAs is
+// merged in one round of loads.
 // Launched as a programmatic dependent of decode_splitkv_kernel: its CTAs may start while the
 // split kernel is still running and wait (griddepcontrol.wait) until that grid has completed
 // and its writes are visible, which hides this launch behind the split kernel.
-constexpr int kMergeWarps = 4;
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
+constexpr int kMergeWarpsSmall = 16, kMergeWarpsLarge = 4;
+template <int kWarps>
+__global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float red_m[kMergeWarps], red_w[kMergeWarps];
-  __shared__ float4 red_o[kMergeWarps][32];
+  __shared__ float red_m[kWarps], red_w[kWarps];
+  __shared__ float4 red_o[kWarps][32];
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p0 = p.ws_prefix[b], p1 = p.ws_prefix[b + 1];
@@ -432,42 +435,59 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   const int W = p.ws_header[0];
   const int c0 = p0 / W, c1 = (p1 - 1) / W;
   if (c0 == c1) return;  // finished inside one CTA
-  // max of the partial LSEs
-  float m = -CUDART_INF_F;
-  for (int c = c0 + threadIdx.x; c <= c1; c += kMergeWarps * 32)
-    m = fmaxf(m, p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red_m[warp] = m;
-  __syncthreads();
-  m = red_m[0];
-#pragma unroll
-  for (int k = 1; k < kMergeWarps; ++k) m = fmaxf(m, red_m[k]);
-  // this warp's partials: c0 + warp, c0 + warp + 4, ...
+  // this warp's partials c0 + warp, c0 + warp + kWarps, ..., four at a time: sum of
+  // 2^(lse_c - m) o_c (lse in log2 units) against a running maximum m, rescaled when m moves
+  const float* lse_src = p.ws_lse + static_cast<int64_t>(b) * kHq + h;
+  const float* o_src = p.ws_o + (static_cast<int64_t>(b) * kHq + h) * kHeadDim + 4 * lane;
+  float m = -CUDART_INF_F, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  const float* src = p.ws_o + (static_cast<int64_t>(b) * kHq + h) * kHeadDim + 4 * lane;
-#pragma unroll 4
-  for (int c = c0 + warp; c <= c1; c += kMergeWarps) {
-    const float w = fast_exp2((p.ws_lse[(static_cast<int64_t>(b) + c) * kHq + h] - m) * kLog2e);
-    const float4 o = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(c) * kHq * kHeadDim);
-    wsum += w;
-    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+  for (int c = c0 + warp; c <= c1; c += 4 * kWarps) {
+    float l2[4];
+    float4 o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int cu = c + u * kWarps;
+      l2[u] = cu <= c1 ? lse_src[static_cast<int64_t>(cu) * kHq] * kLog2e : -CUDART_INF_F;
+      o[u] = cu <= c1 ? *reinterpret_cast<const float4*>(o_src + static_cast<int64_t>(cu) * kHq * kHeadDim)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float mn = fmaxf(fmaxf(m, fmaxf(l2[0], l2[1])), fmaxf(l2[2], l2[3]));
+    const float ms = mn == -CUDART_INF_F ? 0.f : mn;  // no finite partial yet: weights all 0
+    const float sc = fast_exp2(m - ms);
+    acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+    wsum *= sc;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = fast_exp2(l2[u] - ms);
+      wsum += w;
+      acc.x += w * o[u].x; acc.y += w * o[u].y; acc.z += w * o[u].z; acc.w += w * o[u].w;
+    }
+    m = mn;
   }
   red_o[warp][lane] = acc;
-  if (lane == 0) red_w[warp] = wsum;
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_w[warp] = wsum;
+  }
   __syncthreads();
   if (warp != 0) return;
+  float M = red_m[0];
 #pragma unroll
-  for (int k = 1; k < kMergeWarps; ++k) {
+  for (int k = 1; k < kWarps; ++k) M = fmaxf(M, red_m[k]);
+  const float Ms = M == -CUDART_INF_F ? 0.f : M;
+  acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  wsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < kWarps; ++k) {
+    const float s = fast_exp2(red_m[k] - Ms);  // a warp with no partial has m = -inf: s = 0
     const float4 o = red_o[k][lane];
-    acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
-    wsum += red_w[k];
+    acc.x += s * o.x; acc.y += s * o.y; acc.z += s * o.z; acc.w += s * o.w;
+    wsum += s * red_w[k];
   }
   const float inv = 1.0f / wsum;
   *reinterpret_cast<uint2*>(orow) =
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = m + logf(wsum);
+  if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = (M + log2f(wsum)) * kLn2;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -546,8 +566,13 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(decode)");
     // the merge kernel uses no shared memory; giving it the split kernel's carveout keeps the
     // SMs from reconfiguring shared memory / L1 between the two launches of every call
-    e = cudaFuncSetAttribute(decode_merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(decode_merge_kernel<kMergeWarpsSmall>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_merge_kernel<kMergeWarpsLarge>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(decode merge)");
     configured_device = dev;
   }
@@ -577,8 +602,11 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   PA_CHECK_LAUNCH("decode_splitkv_kernel");
   {
     cudaLaunchConfig_t cfg = {};
+    // partials per sequence when the lengths are equal: ceil(grid / batch), plus one for a cut
+    // at each end; more than 4 warps take in one round of 4 loads -> 16 warps per head
+    const bool small = (grid + batch - 1) / batch + 1 > 4 * kMergeWarpsLarge;
     cfg.gridDim = dim3(batch, kHq);
-    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.blockDim = dim3((small ? kMergeWarpsSmall : kMergeWarpsLarge) * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -586,7 +614,8 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, p);
+    cudaError_t e = small ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<kMergeWarpsSmall>, p)
+                          : cudaLaunchKernelEx(&cfg, decode_merge_kernel<kMergeWarpsLarge>, p);
     if (e != cudaSuccess) return record_cuda_error(e, "decode_merge_kernel");
   }
   return PA_OK;
