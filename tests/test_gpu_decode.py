@@ -43,6 +43,19 @@ def test_decode_small(cuda_lib, lens):
     assert cuda_lib.read_device_status(status) == 0
 
 
+@pytest.mark.parametrize("lens", [[1000] * 2, [1000] * 4, [1000] * 8, [5000, 20, 7000]])
+def test_decode_few_sequences_many_partials(cuda_lib, lens):
+    """Few sequences spread over many CTAs, so each is cut into tens of partials and merged by
+    16 warps per head; the last case gives the sequences very different partial counts (two
+    rounds of the warp loop for the longest, one partial for the shortest)."""
+    inp = W.make_paged(91 + len(lens), lens, [1] * len(lens), poison=True, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_decode(cuda_lib, inp, status=status)
+    ref_o, ref_l = oracle_decode(inp)
+    check_attn(out, lse, ref_o, ref_l, what=f"decode {lens}")
+    assert cuda_lib.read_device_status(status) == 0
+
+
 @pytest.mark.parametrize("name,scale_down", [("decode_b16_l27k", 10), ("decode_ragged_b64", 10)])
 def test_decode_reduced_configs(cuda_lib, name, scale_down):
     L, ql = W.lengths_for(name)
