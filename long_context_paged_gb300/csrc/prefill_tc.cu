@@ -34,6 +34,8 @@
 // The running row max moves only when a tile exceeds it by more than 8 (log2 units); O is then
 // rescaled in TMEM by its owning warps; the previous P*V has completed by then, since the
 // commit the warps waited on for this tile's S covers every earlier MMA of the issuer.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -90,6 +92,8 @@ struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
   long long unit_prefix[kMaxBatch + 1];  // first unit of each sequence
   int32_t job_prefix[kMaxBatch + 1];     // first job of each sequence
   int32_t total_jobs;
+  int32_t plan_rounds;                   // whole-job rounds of the balanced split
+  long long plan_u0, plan_u1;            // this CTA's range of the remaining units
 };
 
 static_assert(sizeof(PrefillTcSmem) + 1024 <= 232448, "prefill shared memory over the 227 KB limit");
@@ -105,10 +109,11 @@ struct PrefillTcParams {
   uint16_t* out;
   float* lse;
   int32_t* status;
-  long long* ws_header;   // [0] tail units per CTA, [1] total units, [2] first tail unit,
-                          // [3] jobs done whole in the round-robin phase
+  long long* ws_header;   // [0] grid size, [1] total units, [2] first unit after the whole
+                          // jobs, [3] jobs done whole in the round-robin phase
   long long* ws_prefix;   // [batch + 1] first unit of each sequence
   int32_t* ws_job_prefix; // [batch + 1] first job of each sequence
+  long long* ws_tail;     // [grid + 1] first unit of each CTA's range after the whole jobs
   uint8_t* ws_records;    // [2 * grid][kRecordBytes]
 };
 
@@ -159,9 +164,9 @@ struct Piece {
 
 // The pieces one CTA owns, in order: first whole jobs c, c + G, c + 2G, ... (G = grid size) for
 // `rounds` rounds, all CTAs starting at key tile 0 together so that the CTAs of one KV head stream
-// the same K/V tiles through L2 at about the same time; then an equal share [U0, U1) of the
-// units of the remaining jobs, whose first and last pieces may be parts of jobs shared with
-// neighbouring CTAs.
+// the same K/V tiles through L2 at about the same time; then a range [U0, U1) of the units of the
+// remaining jobs (sized by plan_split so that every CTA ends with the same number of units),
+// whose first and last pieces may be parts of jobs shared with neighbouring CTAs.
 struct JobWalker {
   const PrefillTcParams* p;
   const long long* prefix;
@@ -324,6 +329,90 @@ __device__ void build_unit_prefix(const PrefillTcParams& p, PrefillTcSmem& s) {
   __syncthreads();
 }
 
+// Units (key tiles) of job jo: jobs are numbered sequence by sequence, then KV head, then q tile.
+__device__ long long job_units(const PrefillTcParams& p, const PrefillTcSmem& s, int jo) {
+  int lo = 0, hi = p.batch;  // last b with job_prefix[b] <= jo (a sequence that has jobs)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.job_prefix[mid] <= jo) lo = mid; else hi = mid;
+  }
+  const SeqGeom g = seq_geom(p, lo, false);
+  return tiles_of(g, (jo - s.job_prefix[lo]) % g.nqt);
+}
+
+// Balanced split of all units over the G CTAs (G <= kThreads, one CTA per thread here). With
+// target = ceil(total / G): whole jobs go round-robin (CTA c takes jobs c, c + G, ...) for as many
+// rounds as keep every CTA's whole-job units within target; the units of the remaining jobs are
+// then cut into consecutive ranges, CTA c's of size target - whole(c), so CTAs whose whole jobs were
+// short take more of the rest and all end level even when job lengths differ widely (chunks of
+// different lengths and offsets in one call). Every CTA computes the same plan; CTA 0 also
+// publishes the range starts for the merge kernel.
+__device__ void plan_split(const PrefillTcParams& p, PrefillTcSmem& s, int G, int& rounds,
+                           long long& T0, long long& U0, long long& U1) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long total = s.total_units;
+  const long long target = (total + G - 1) / G;
+  const int rmax = s.total_jobs / G;
+  if (tid == 0) s.plan_rounds = rmax;
+  __syncthreads();
+  if (tid < G) {
+    long long acc = 0;
+    int r = 0;
+    for (; r < rmax; ++r) {
+      acc += job_units(p, s, tid + r * G);
+      if (acc > target) break;
+    }
+    if (r < rmax) atomicMin(&s.plan_rounds, r);
+  }
+  __syncthreads();
+  rounds = s.plan_rounds;
+  long long tail = 0;
+  if (tid < G) {
+    long long whole = 0;
+    for (int r = 0; r < rounds; ++r) whole += job_units(p, s, tid + r * G);
+    tail = target - whole;  // >= 0: every CTA's whole jobs fit in target for this many rounds
+  }
+  // exclusive scan of the range sizes over the CTAs
+  const long long incl = warp_incl_scan64(tail, lane);
+  if (lane == 31) s.warp_sums[warp] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    long long run = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const long long v = s.warp_sums[w];
+      s.warp_sums[w] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  const long long excl = s.warp_sums[warp] + incl - tail;
+  // first unit after the whole jobs: that of job rounds * G
+  const int n_dp = rounds * G;
+  T0 = total;
+  if (n_dp < s.total_jobs) {
+    int lo = 0, hi = p.batch;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s.job_prefix[mid] <= n_dp) lo = mid; else hi = mid;
+    }
+    const SeqGeom g0 = seq_geom(p, lo, false);
+    const int rem = n_dp - s.job_prefix[lo];
+    T0 = s.unit_prefix[lo] + (rem / g0.nqt) * g0.T + units_before(g0, rem % g0.nqt);
+  }
+  if (tid < G) {
+    const long long u0 = min(total, T0 + excl), u1 = min(total, T0 + excl + tail);
+    if (tid == static_cast<int>(blockIdx.x)) {
+      s.plan_u0 = u0;
+      s.plan_u1 = u1;
+    }
+    if (blockIdx.x == 0) p.ws_tail[tid] = u0;
+  }
+  if (blockIdx.x == 0 && tid == 0) p.ws_tail[G] = total;
+  __syncthreads();
+  U0 = s.plan_u0;
+  U1 = s.plan_u1;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap k_map,
@@ -337,33 +426,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   build_unit_prefix(p, s);
   const long long total = s.total_units;
   const int G = gridDim.x;
-  const int rounds = s.total_jobs / G;            // whole-job rounds (every CTA one job each)
-  const int n_dp = rounds * G;
-  long long T0 = total;                           // first unit of job n_dp
-  if (n_dp < s.total_jobs) {
-    int lo = 0, hi = p.batch;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s.job_prefix[mid] <= n_dp) lo = mid; else hi = mid;
-    }
-    const SeqGeom g0 = seq_geom(p, lo, false);
-    const int rem = n_dp - s.job_prefix[lo];
-    T0 = s.unit_prefix[lo] + (rem / g0.nqt) * g0.T + units_before(g0, rem % g0.nqt);
-  }
-  const long long Wt = (total - T0 + G - 1) / G;  // tail units per CTA
+  int rounds;
+  long long T0, U0, U1;
+  plan_split(p, s, G, rounds, T0, U0, U1);
   if (blockIdx.x == 0) {
     if (threadIdx.x == 0) {
-      p.ws_header[0] = Wt;
+      p.ws_header[0] = G;
       p.ws_header[1] = total;
       p.ws_header[2] = T0;
-      p.ws_header[3] = n_dp;
+      p.ws_header[3] = static_cast<long long>(rounds) * G;
     }
     for (int b = threadIdx.x; b <= p.batch; b += kThreads) {
       p.ws_prefix[b] = s.unit_prefix[b];
       p.ws_job_prefix[b] = s.job_prefix[b];
     }
   }
-  const long long U0 = T0 + blockIdx.x * Wt, U1 = min(total, U0 + Wt);
   if (rounds == 0 && U0 >= U1) return;  // uniform across the CTA: nothing allocated yet
 
   if (threadIdx.x == 0) {
@@ -776,25 +853,39 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
   if (qt >= s.nqt) return;
   const int jo = p.ws_job_prefix[b] + g * s.nqt + qt;
   if (jo < p.ws_header[3]) return;  // done whole in the round-robin phase
-  const long long Wt = p.ws_header[0], T0 = p.ws_header[2];
+  const int G = static_cast<int>(p.ws_header[0]);
   const long long u0 = p.ws_prefix[b] + g * s.T + units_before(s, qt);
   const long long J = tiles_of(s, qt);
-  const long long c0 = (u0 - T0) / Wt, c1 = (u0 + J - 1 - T0) / Wt;
+  // the CTA whose range [ws_tail[c], ws_tail[c + 1]) holds unit u (the last c with a start <= u:
+  // a CTA with an empty range shares its start with the next one)
+  auto cta_of = [&](long long u) {
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.ws_tail[mid] <= u) lo = mid; else hi = mid;
+    }
+    return lo;
+  };
+  const int c0 = cta_of(u0), c1 = cta_of(u0 + J - 1);
   if (c0 == c1) return;
   const int t = threadIdx.x >> 7, r = threadIdx.x & 127;
   const int qrow = qt * kTileM + r;
   if (qrow >= s.n) return;
-  auto rec_of = [&](long long c) {
+  // the piece in CTA c0 starts the job (slot 1); later CTAs hold continuations (slot 0); CTAs with
+  // an empty range in between hold nothing
+  auto rec_of = [&](int c) {
     return p.ws_records + (2 * static_cast<size_t>(c) + (c == c0 ? 1 : 0)) * kRecordBytes;
   };
+  auto empty_range = [&](int c) { return p.ws_tail[c] == p.ws_tail[c + 1]; };
   float m = -CUDART_INF_F;
-  for (long long c = c0; c <= c1; ++c)
-    m = fmaxf(m, reinterpret_cast<const float*>(rec_of(c) + kRecordO)[t * 128 + r]);
+  for (int c = c0; c <= c1; ++c)
+    if (!empty_range(c)) m = fmaxf(m, reinterpret_cast<const float*>(rec_of(c) + kRecordO)[t * 128 + r]);
   float acc[kHeadDim];
 #pragma unroll
   for (int d = 0; d < kHeadDim; ++d) acc[d] = 0.f;
   float sum = 0.f;
-  for (long long c = c0; c <= c1; ++c) {
+  for (int c = c0; c <= c1; ++c) {
+    if (empty_range(c)) continue;
     const uint8_t* rec = rec_of(c);
     const float lp = reinterpret_cast<const float*>(rec + kRecordO)[t * 128 + r];
     if (lp == -CUDART_INF_F) continue;  // the piece held no key visible to this row
@@ -831,7 +922,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct PrefillWs {
-  size_t header, prefix, job_prefix, records, total;
+  size_t header, prefix, job_prefix, tail, records, total;
 };
 
 PrefillWs prefill_ws(int batch, int grid) {
@@ -839,15 +930,19 @@ PrefillWs prefill_ws(int batch, int grid) {
   w.header = 0;
   w.prefix = 256;
   w.job_prefix = align256(w.prefix + sizeof(long long) * (batch + 1));
-  w.records = align256(w.job_prefix + sizeof(int32_t) * (batch + 1));
+  w.tail = align256(w.job_prefix + sizeof(int32_t) * (batch + 1));
+  w.records = align256(w.tail + sizeof(long long) * (grid + 1));
   w.total = align256(w.records + 2 * static_cast<size_t>(grid) * kRecordBytes);
   return w;
 }
 
+// One persistent CTA per SM; plan_split gives each CTA one thread of its CTA, so at most kThreads.
+int prefill_grid() { return std::min(sm_count_current_device(), kThreads); }
+
 }  // namespace
 
 size_t prefill_workspace_bytes(int batch) {
-  const int grid = sm_count_current_device();
+  const int grid = prefill_grid();
   if (grid <= 0 || batch < 0) return 0;
   return prefill_ws(batch, grid).total;
 }
@@ -863,7 +958,7 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
     return PA_ERR_UNSUPPORTED;
   }
   if (num_pages * kPage >= (int64_t(1) << 31) || total_q >= (1 << 24)) return PA_ERR_UNSUPPORTED;
-  const int grid = sm_count_current_device();
+  const int grid = prefill_grid();
   if (grid <= 0) return PA_ERR_CUDA;
   const PrefillWs w = prefill_ws(batch, grid);
   if (workspace == nullptr || workspace_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
@@ -914,6 +1009,7 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   p.ws_header = reinterpret_cast<long long*>(ws + w.header);
   p.ws_prefix = reinterpret_cast<long long*>(ws + w.prefix);
   p.ws_job_prefix = reinterpret_cast<int32_t*>(ws + w.job_prefix);
+  p.ws_tail = reinterpret_cast<long long*>(ws + w.tail);
   p.ws_records = ws + w.records;
   prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(qm, km, vm, p);
   PA_CHECK_LAUNCH("prefill_tc_kernel");
