@@ -93,6 +93,27 @@ def test_prefill_ragged_mix_full_size(cuda_lib):
     assert cuda_lib.read_device_status(status) == 0
 
 
+def test_prefill_uneven_jobs_level_split(cuda_lib):
+    """Chunks whose jobs differ in length (515 / 1,024 / 1,024 / 128 queries at offsets 33,783 /
+    36,652 / 26,147 / 31,557). On a 152-SM GB300 the levelled work split gives several CTAs
+    whole jobs that exactly fill their share, so their second-phase ranges are empty and lie
+    inside jobs cut across many CTAs (the third chunk's query tiles 5 and 6 of KV head 6), which
+    the merge must skip. Every row of those tiles and sampled rows of the rest are checked."""
+    q_lens = [515, 1024, 1024, 128]
+    seq_lens = [34_298, 37_676, 27_171, 31_685]
+    inp = W.make_paged(203, seq_lens, q_lens, poison=True, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefill(cuda_lib, inp, status=status)
+    cu = host(inp.cu_q_lens)
+    rows = set(int(cu[2]) + r for r in range(5 * 128, 7 * 128))
+    for b in range(len(q_lens)):
+        rows |= {int(cu[b]) + r for r in sampled_rows(q_lens[b], 20 + b, count=16)}
+    rows = sorted(rows)
+    ref_o, ref_l = oracle_prefill(inp, rows=rows)
+    check_attn(out, lse, ref_o, ref_l, rows=rows, what="uneven jobs, levelled split")
+    assert cuda_lib.read_device_status(status) == 0
+
+
 def test_prefill_chunk_longer_than_sequence_is_flagged(cuda_lib):
     inp = W.make_paged(202, [50], [20], device="cuda")
     sl = inp.seq_lens.clone()
