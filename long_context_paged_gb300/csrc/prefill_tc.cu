@@ -63,6 +63,11 @@ constexpr uint32_t kTileBytes = 2 * kBlockBytes;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxBatch = 128;   // chunks per call (the unit prefix lives in shared memory)
 constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more stage in flight
+// Fixed cost of a job beyond its key tiles, in tiles: its epilogue and the restart of the
+// softmax -> P -> P*V chain on its first tile (measured ~5.5 us a job, about 3 tiles). In the
+// work split each job occupies its key tiles followed by this many cost units, so that a CTA whose
+// share holds many short jobs is not overloaded; the cost units hold no key tile.
+constexpr int kJobCost = 3;
 // Register split: the two softmax warpgroups grow to 200 registers per thread, the
 // producer/MMA warpgroup shrinks to 104 (at 72 the issuer's loop spilled and starved the tensor
 // pipe; softmax below ~200 spills); 256 * 200 + 128 * 104 = 64,512 = 384 threads x 168, the
@@ -142,15 +147,16 @@ __device__ __forceinline__ SeqGeom seq_geom(const PrefillTcParams& p, int b, boo
   s.a = (s.off + kTileN - 1) / kTileN + 1;
   s.Jlast = (s.off + s.n - 1) / kTileN + 1;
   const long long full = s.nqt - 1;
-  s.T = full * s.a + full * (full - 1) / 2 + s.Jlast;
+  s.T = full * s.a + full * (full - 1) / 2 + s.Jlast + static_cast<long long>(s.nqt) * kJobCost;
   return s;
 }
 
 __device__ __forceinline__ long long tiles_of(const SeqGeom& s, int qt) {
   return qt < s.nqt - 1 ? s.a + qt : s.Jlast;
 }
+// Units of the jobs before q tile qt of one head: their key tiles and their cost units.
 __device__ __forceinline__ long long units_before(const SeqGeom& s, int qt) {
-  return static_cast<long long>(qt) * s.a + static_cast<long long>(qt) * (qt - 1) / 2;
+  return static_cast<long long>(qt) * (s.a + kJobCost) + static_cast<long long>(qt) * (qt - 1) / 2;
 }
 
 // One job piece this CTA owns: key tiles [jb, je) of job (b, g, qt).
@@ -224,6 +230,8 @@ struct JobWalker {
     int qt = 0;
     while (qt + 1 < s.nqt && units_before(s, qt + 1) <= rem2) ++qt;
     set(lo, g, qt, prefix[lo] + g * s.T + units_before(s, qt), s);
+    // a range that starts in the cost units after a job's last key tile holds none of its tiles
+    if (!cur.valid && cur.u0 + cur.J + kJobCost < U1) advance_tail();
   }
 
   __device__ void start(const PrefillTcParams& pp, const long long* pre, const int32_t* jpre,
@@ -246,7 +254,12 @@ struct JobWalker {
       else start_tail();
       return;
     }
-    long long u0 = cur.u0 + cur.J;
+    advance_tail();
+  }
+
+  // the job after cur in unit order (the tail phase walks its range job by job)
+  __device__ void advance_tail() {
+    long long u0 = cur.u0 + cur.J + kJobCost;
     int b = cur.b, g = cur.g, qt = cur.qt + 1;
     SeqGeom s = cur.s;
     if (qt >= s.nqt) {
@@ -329,7 +342,8 @@ __device__ void build_unit_prefix(const PrefillTcParams& p, PrefillTcSmem& s) {
   __syncthreads();
 }
 
-// Units (key tiles) of job jo: jobs are numbered sequence by sequence, then KV head, then q tile.
+// Units of job jo (its key tiles plus kJobCost): jobs are numbered sequence by sequence, then KV
+// head, then q tile.
 __device__ long long job_units(const PrefillTcParams& p, const PrefillTcSmem& s, int jo) {
   int lo = 0, hi = p.batch;  // last b with job_prefix[b] <= jo (a sequence that has jobs)
   while (hi - lo > 1) {
@@ -337,7 +351,7 @@ __device__ long long job_units(const PrefillTcParams& p, const PrefillTcSmem& s,
     if (s.job_prefix[mid] <= jo) lo = mid; else hi = mid;
   }
   const SeqGeom g = seq_geom(p, lo, false);
-  return tiles_of(g, (jo - s.job_prefix[lo]) % g.nqt);
+  return tiles_of(g, (jo - s.job_prefix[lo]) % g.nqt) + kJobCost;
 }
 
 // Balanced split of all units over the G CTAs (G <= kThreads, one CTA per thread here). With
