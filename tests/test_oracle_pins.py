@@ -400,6 +400,31 @@ MUTANTS = {
 }
 
 
+def _mutant_append(slot_shift=0, ignore_start=False, identity_pages=False, swap_kv=False):
+    """The oracle's kv_append with one step changed (for the planted-mistake test only)."""
+    def kv_append(k_new, v_new, cu_new_lens, start_pos, block_table, k_pool, v_pool):
+        k_out, v_out = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+        P = k_pool.shape[1]
+        cu = [int(c) for c in cu_new_lens]
+        for b in range(len(cu) - 1):
+            for j in range(cu[b + 1] - cu[b]):
+                pos = (0 if ignore_start else int(start_pos[b])) + j + slot_shift
+                page = pos // P if identity_pages else int(block_table[b, pos // P])
+                src_k, src_v = (v_new, k_new) if swap_kv else (k_new, v_new)
+                k_out[page, pos % P] = src_k[cu[b] + j]
+                v_out[page, pos % P] = src_v[cu[b] + j]
+        return k_out, v_out
+    return kv_append
+
+
+MUTANTS.update({
+    "append_slot_off_by_one": lambda m: m.setattr(oracle, "kv_append", _mutant_append(slot_shift=1)),
+    "append_start_ignored": lambda m: m.setattr(oracle, "kv_append", _mutant_append(ignore_start=True)),
+    "append_block_table_bypassed": lambda m: m.setattr(oracle, "kv_append", _mutant_append(identity_pages=True)),
+    "append_k_v_swapped": lambda m: m.setattr(oracle, "kv_append", _mutant_append(swap_kv=True)),
+})
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_planted_mistake_is_caught(name, monkeypatch):
     assert _all_golden_pass()
@@ -408,6 +433,6 @@ def test_planted_mistake_is_caught(name, monkeypatch):
         with np.errstate(all="ignore"):
             try:
                 caught = not _all_golden_pass()
-            except Exception:
+            except (AssertionError, IndexError, ValueError):
                 caught = True
     assert caught, f"planted mistake {name} passed every golden pin"
