@@ -77,6 +77,46 @@ def test_argument_errors_are_rejected_before_launch(lib):
     assert lib.pa_read_device_status(null, null, null) == 1
 
 
+def test_prefill_argument_errors_are_rejected_before_launch(lib):
+    """attn_prefill_chunk's checks, each before any CUDA call. Every case here must be rejected:
+    the pointers are fake (aligned, non-null host addresses) and are never dereferenced."""
+    import long_context_paged_gb300 as pa
+    good = pa.Dims(*pa.DEFAULT_DIMS)
+    null = None
+    a = ctypes.c_void_p(1 << 20)     # fake 16-byte-aligned address
+    mis = ctypes.c_void_p((1 << 20) + 8)
+
+    def call(q=a, cu=a, total_q=128, k=a, v=a, num_pages=64, bt=a, bt_stride=8, sl=a, batch=1,
+             max_q=128, max_s=1024, scale=0.0884, out=a):
+        return lib.attn_prefill_chunk(good, q, cu, total_q, k, v, num_pages, bt, bt_stride, sl,
+                                      batch, max_q, max_s, scale, out, null, null, 0, null, null)
+
+    INVALID, UNSUPPORTED, OK = 1, 2, 0
+    # sizes and scale
+    assert call(batch=-1) == INVALID
+    assert call(total_q=-1) == INVALID
+    assert call(bt_stride=0) == INVALID
+    assert call(num_pages=0) == INVALID
+    assert call(max_q=-1) == INVALID
+    assert call(max_q=2048, max_s=1024) == INVALID          # chunk longer than any sequence
+    assert call(max_s=131073) == INVALID                    # past the 128K context
+    for scale in (0.0, -1.0, float("nan"), float("inf")):
+        assert call(scale=scale) == INVALID
+    # missing or misaligned pointers
+    for kw in ("q", "cu", "k", "v", "bt", "sl", "out"):
+        assert call(**{kw: null}) == INVALID, kw
+    for kw in ("q", "k", "v", "out"):
+        assert call(**{kw: mis}) == INVALID, kw
+    # limits of the kernel
+    assert call(batch=129, max_q=1, total_q=129) == UNSUPPORTED   # at most 128 chunks per call
+    assert call(total_q=1 << 24) == UNSUPPORTED
+    assert call(num_pages=1 << 27) == UNSUPPORTED                # token index past 2^31
+    # empty work is a no-op success, whatever the pointers
+    assert call(batch=0, q=null, out=null) == OK
+    assert call(total_q=0, q=null, out=null) == OK
+    assert call(max_q=0, q=null, out=null) == OK
+
+
 def test_adaptor_argument_errors_are_rejected_before_launch(lib):
     """adaptor_mlp_merge4 validates everything on the host; the fake pointers below are never
     dereferenced because every case returns before anything is launched."""
