@@ -108,6 +108,7 @@ pa_status kv_append_paged(pa_dims dims, const void* k_new, const void* v_new, in
  *   seq_lens     int32 [batch], keys per sequence (0 allowed: o = 0, lse = -inf)
  *   max_seq_len  host upper bound of seq_lens (<= 131072, the 128K context); a larger
  *                device value is cut to bt_stride*16 and flagged
+ *   softmax_scale  any value but NaN (PA_ERR_INVALID_ARG); 1/sqrt(128) for this model
  *   out          bf16 [batch][Hq][128];  lse fp32 [batch][Hq] or NULL
  *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes, 256-byte
  *                aligned; holds per-split partial results. Calls that share a workspace must
@@ -161,6 +162,8 @@ pa_status attn_decode_paged_noalloc(pa_dims dims, const void* q, const void* k_p
  *   seq_lens    int32 [batch]: keys of sequence b INCLUDING the chunk (appended first)
  *   batch       number of chunks, at most 128 per call
  *   max_q_len   host upper bound of the chunk lengths
+ *   softmax_scale  0 < scale < 1e30, else PA_ERR_INVALID_ARG (the causal mask sets raw
+ *               scores to -inf before scaling, which needs a positive, finite scale)
  * Query i of chunk b (length n) sits at position seq_lens[b] - n + i and sees keys
  * 0 .. seq_lens[b] - n + i (bottom-right causal alignment). A chunk longer than its sequence
  * is flagged and produces nothing.

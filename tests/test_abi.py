@@ -117,6 +117,53 @@ def test_prefill_argument_errors_are_rejected_before_launch(lib):
     assert call(max_q=0, q=null, out=null) == OK
 
 
+def test_decode_and_append_argument_errors_are_rejected_before_launch(lib):
+    """attn_decode_paged and kv_append_paged checks, each before any CUDA call. Every case here
+    must be rejected: the pointers are fake (aligned, non-null host addresses), never read."""
+    import long_context_paged_gb300 as pa
+    good = pa.Dims(*pa.DEFAULT_DIMS)
+    null = None
+    a = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 21)    # 256-byte aligned
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    INVALID, OK = 1, 0
+
+    def decode(q=a, k=a, v=a, num_pages=64, bt=a, bt_stride=8, sl=a, batch=1, max_s=1024,
+               scale=0.0884, out=a, work=ws):
+        return lib.attn_decode_paged(good, q, k, v, num_pages, bt, bt_stride, sl, batch, max_s,
+                                     scale, out, null, work, 1 << 30, null, null)
+
+    assert decode(batch=-1) == INVALID
+    assert decode(batch=4097) == INVALID                    # past the largest decode batch
+    assert decode(bt_stride=0) == INVALID
+    assert decode(num_pages=0) == INVALID
+    assert decode(max_s=-1) == INVALID
+    assert decode(max_s=131073) == INVALID
+    assert decode(scale=float("nan")) == INVALID
+    for kw in ("q", "k", "v", "bt", "sl", "out", "work"):
+        assert decode(**{kw: null}) == INVALID, kw
+    for kw in ("q", "k", "v", "out"):
+        assert decode(**{kw: mis}) == INVALID, kw
+    assert decode(work=ctypes.c_void_p((1 << 21) + 128)) == INVALID   # workspace not 256-aligned
+    assert decode(batch=0, q=null, work=null) == OK
+
+    def append(k_new=a, v_new=a, total=16, cu=a, start=a, batch=1, bt=a, bt_stride=8, kp=a,
+               vp=a, num_pages=64):
+        return lib.kv_append_paged(good, k_new, v_new, total, cu, start, batch, bt, bt_stride,
+                                   kp, vp, num_pages, null, null)
+
+    assert append(total=-1) == INVALID
+    assert append(batch=-1) == INVALID
+    assert append(bt_stride=0) == INVALID
+    assert append(num_pages=0) == INVALID
+    for kw in ("k_new", "v_new", "cu", "start", "bt", "kp", "vp"):
+        assert append(**{kw: null}) == INVALID, kw
+    for kw in ("k_new", "v_new", "kp", "vp"):
+        assert append(**{kw: mis}) == INVALID, kw
+    assert append(total=0, k_new=null) == OK
+    assert append(batch=0, k_new=null) == OK
+
+
 def test_adaptor_argument_errors_are_rejected_before_launch(lib):
     """adaptor_mlp_merge4 validates everything on the host; the fake pointers below are never
     dereferenced because every case returns before anything is launched."""
