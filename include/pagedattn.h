@@ -89,8 +89,10 @@ typedef struct pa_dims {
  *   block_table    int32 [batch][bt_stride]; must already cover the new positions
  *   k_pool, v_pool bf16 [num_pages][16][Hkv][128], written in place
  * Row j of sequence b goes to position start_pos[b] + j. The copy is bit-exact; no other
- * pool byte changes. Rows at or past cu_new_lens[batch] are ignored. A position whose table
- * entry is missing (past bt_stride) or out of range is skipped and flagged.
+ * pool byte changes. Rows at or past cu_new_lens[batch] are ignored. If cu_new_lens[batch]
+ * exceeds total_new, only the first total_new rows are written and PA_DEV_ERR_LENGTH is set.
+ * A position whose table entry is missing (past bt_stride) or out of range is skipped and
+ * flagged.
  * ------------------------------------------------------------------------------------------ */
 pa_status kv_append_paged(pa_dims dims, const void* k_new, const void* v_new, int32_t total_new,
                           const int32_t* cu_new_lens, const int32_t* start_pos, int32_t batch,
@@ -110,19 +112,29 @@ pa_status kv_append_paged(pa_dims dims, const void* k_new, const void* v_new, in
  *                device value is cut to bt_stride*16 and flagged
  *   softmax_scale  any value but NaN (PA_ERR_INVALID_ARG); 1/sqrt(128) for this model
  *   out          bf16 [batch][Hq][128];  lse fp32 [batch][Hq] or NULL
- *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes, 256-byte
- *                aligned; holds per-split partial results. Calls that share a workspace must
- *                not overlap on the GPU.
- * The key range of all sequences is cut into equal page ranges, one per resident CTA
- * (split-KV); partial (o, lse) pairs of sequences that span ranges are merged by log-sum-exp.
+ *   split_tokens   keys per split-KV range, rounded up to whole 16-token pages; 0 = auto (one
+ *                equal share of all sequences' pages per SM). With a split size the ranges
+ *                are that long (the last one shorter), raised if needed so that there are at
+ *                most 64 ranges per SM; any value >= the batch's total keys gives one range.
+ *                Negative: PA_ERR_INVALID_ARG. The result does not depend on it beyond
+ *                rounding (the split-KV partials are merged exactly by log-sum-exp).
+ *   out          bf16 [batch][Hq][128];  lse fp32 [batch][Hq] or NULL
+ *   workspace    device scratch of at least pa_decode_workspace_size(dims, batch, max_seq_len,
+ *                split_tokens) bytes, 256-byte aligned; holds per-split partial results. With
+ *                split_tokens = 0 the size does not depend on max_seq_len. Calls that share a
+ *                workspace must not overlap on the GPU.
+ * The key range of all sequences is laid end to end and cut into page ranges (split-KV);
+ * partial (o, lse) pairs of sequences that span ranges are merged by log-sum-exp.
  * ------------------------------------------------------------------------------------------ */
-size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len);
+size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len,
+                                int32_t split_tokens);
 
 pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool, const void* v_pool,
                             int64_t num_pages, const int32_t* block_table, int32_t bt_stride,
                             const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
-                            float softmax_scale, void* out, float* lse, void* workspace,
-                            size_t workspace_bytes, int32_t* status, pa_stream_t stream);
+                            float softmax_scale, int32_t split_tokens, void* out, float* lse,
+                            void* workspace, size_t workspace_bytes, int32_t* status,
+                            pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * attn_decode_paged_noalloc — attn_decode_paged without a caller-provided workspace.
@@ -134,12 +146,18 @@ pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool, con
  * the pools, block_table, seq_lens, out and lse exactly as for attn_decode_paged; this call
  * itself allocates nothing and calls no allocating routine.
  *
- * Scratch lives in one fixed 4.5 MiB device array inside the library; every GPU that loads the
- * library holds it until the process exits. Limit: pa_decode_workspace_size(dims, batch, ...)
- * must not exceed 4.5 MiB (batch up to about 400 on a 152-SM GB300); larger batches return
- * PA_ERR_WORKSPACE_TOO_SMALL with the sizes in pa_last_error().
+ * The split size is automatic (split_tokens = 0 of attn_decode_paged).
+ * Scratch lives in one fixed 4.5 MiB device array inside the library, held until the process
+ * exits by every GPU on which the library's decode code has been loaded. Limit:
+ * pa_decode_workspace_size(dims, batch, max_seq_len, 0) must not exceed 4.5 MiB (batch up to
+ * about 400 on a 152-SM GB300); larger batches return PA_ERR_WORKSPACE_TOO_SMALL with the
+ * sizes in pa_last_error().
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current) and caches it; make that first call before any stream capture.
+ * with that device current) and caches it. Under CUDA's default lazy module loading that is
+ * also when the device code of this part of the library is loaded and the 4.5 MiB are
+ * committed on the device, unless an earlier call of attn_decode_paged on that device already
+ * loaded it. So make the first call before reserving all free device memory for something
+ * else, and before any stream capture; a call with batch = 0 does only this set-up.
  * Every call shares the one array and no call needs it zeroed (each call writes every scratch
  * byte it later reads), so calls that overlap on the GPU (different streams, or several host
  * threads) race on it and must be serialized by the caller.
@@ -228,6 +246,17 @@ pa_status adaptor_mlp_merge4(int32_t num_frames, const void* frames, const void*
                              const float* gamma, const float* beta, float eps, void* out,
                              void* workspace, size_t workspace_bytes, int32_t* status,
                              pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * pa_debug_decode_starve — test hook for the bounded waits; never needed in production.
+ *
+ * With enable != 0, every later attn_decode_paged launch made by the calling host thread bounds
+ * each of its mbarrier waits by 1 ms (instead of 2 s) and leaves the first ring stage of CTA 0
+ * unfilled, so that CTA's consumer warps give up waiting, set PA_DEV_ERR_TIMEOUT in *status and
+ * return (the producer drains its copies first; the decode kernels hold no tensor-memory
+ * state). The output of such a call is undefined. enable = 0 restores normal launches.
+ * ------------------------------------------------------------------------------------------ */
+pa_status pa_debug_decode_starve(int32_t enable);
 
 /* Read and clear the device status word: waits for `stream`, copies *status to *flags_out,
  * then zeroes it. */

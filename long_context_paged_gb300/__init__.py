@@ -22,7 +22,7 @@ __all__ = [
     "load", "PagedAttnError", "Dims", "DEFAULT_DIMS",
     "kv_append_paged", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_prefill_chunk",
     "attn_merge_lse", "adaptor_mlp_merge4", "adaptor_workspace_size",
-    "decode_workspace_size", "prefill_workspace_size", "read_device_status",
+    "decode_workspace_size", "prefill_workspace_size", "read_device_status", "debug_decode_starve",
     "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "lib_path",
 ]
 
@@ -63,9 +63,10 @@ _F = ctypes.c_float
 
 _SIGS = {
     "kv_append_paged": (_I32, [Dims, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _I64, _P, _P]),
-    "pa_decode_workspace_size": (_SZ, [Dims, _I32, _I32]),
-    "attn_decode_paged": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _P, _P, _P,
-                                 _SZ, _P, _P]),
+    "pa_decode_workspace_size": (_SZ, [Dims, _I32, _I32, _I32]),
+    "attn_decode_paged": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _I32, _P, _P,
+                                 _P, _SZ, _P, _P]),
+    "pa_debug_decode_starve": (_I32, [_I32]),
     "attn_decode_paged_noalloc": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _P,
                                          _P, _P, _P]),
     "pa_prefill_workspace_size": (_SZ, [Dims, _I32, _I32, _I32]),
@@ -151,8 +152,8 @@ def kv_append_paged(k_new, v_new, cu_new_lens, start_pos, block_table, k_pool, v
         k_pool.shape[0], _ptr(status), _stream(stream)))
 
 
-def decode_workspace_size(batch: int, max_seq_len: int, dims=None) -> int:
-    return int(load().pa_decode_workspace_size(_dims(dims), batch, max_seq_len))
+def decode_workspace_size(batch: int, max_seq_len: int, split_tokens: int = 0, dims=None) -> int:
+    return int(load().pa_decode_workspace_size(_dims(dims), batch, max_seq_len, split_tokens))
 
 
 def prefill_workspace_size(batch: int, max_q_len: int, max_seq_len: int, dims=None) -> int:
@@ -166,9 +167,11 @@ def _workspace(nbytes, device, workspace):
 
 
 def attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int,
-                      softmax_scale: float, *, out=None, lse=None, workspace=None, status=None,
-                      stream=None, want_lse=True, dims=None):
-    """Decode attention: q [B, Hq, D] over each sequence's cached keys. Returns (out, lse)."""
+                      softmax_scale: float, *, split_tokens: int = 0, out=None, lse=None,
+                      workspace=None, status=None, stream=None, want_lse=True, dims=None):
+    """Decode attention: q [B, Hq, D] over each sequence's cached keys. Returns (out, lse).
+
+    split_tokens: keys per split-KV range (whole pages); 0 = one equal share per SM."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_pool, "k_pool", torch.bfloat16, 4)
     _need(v_pool, "v_pool", torch.bfloat16, 4)
@@ -179,14 +182,14 @@ def attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty(B, q.shape[1], dtype=torch.float32, device=q.device)
-    ws_bytes = decode_workspace_size(B, max_seq_len, dims)
+    ws_bytes = decode_workspace_size(B, max_seq_len, split_tokens, dims)
     workspace = _workspace(ws_bytes, q.device, workspace)
     lib = load()
     _check("attn_decode_paged", lib.attn_decode_paged(
         _dims(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), float(softmax_scale),
-        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _ptr(status), _stream(stream)))
+        int(split_tokens), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
     return out, lse
 
 
@@ -281,6 +284,12 @@ def adaptor_mlp_merge4(frames, w1, b1, w2, b2, gamma, beta, eps: float = 1e-5, *
         float(eps), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
     return out
+
+
+def debug_decode_starve(enable: bool) -> None:
+    """Test hook: later decode launches of this thread leave one ring stage empty and bound
+    their waits by 1 ms, so the bounded-wait give-up path runs (status PA_DEV_ERR_TIMEOUT)."""
+    _check("pa_debug_decode_starve", load().pa_debug_decode_starve(1 if enable else 0))
 
 
 def read_device_status(status, stream=None) -> int:

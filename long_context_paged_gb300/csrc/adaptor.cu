@@ -13,12 +13,12 @@
 // through a 4-stage TMA ring (A 16 KB + B 32 KB per stage, 128-byte swizzle), fp32
 // accumulators in two 256-column TMEM buffers so the epilogue of one tile overlaps the MMAs of
 // the next. Warps: 0-3 epilogue (bias, SiLU, bf16, store), 4 TMA producer, 5 MMA issuer.
-// At K = 4096 a tile pulls 3 MB through L2, which bounds the main loop, so CTAs run in
-// clusters of two on row tiles 2i, 2i + 1 of the same column tile: each loads its own A and
-// half of the shared B tile, multicast into both CTAs' shared memory (2 MB per tile instead of
-// 3); a stage is refilled once both CTAs' MMAs have released it (their commits arrive on both
-// CTAs' barriers).
+// Tiles are numbered row tile by row tile, so the CTAs that run the column tiles of one row
+// tile at the same time read its A rows from L2 once they are in; the weights (8 MB and 2 MB)
+// stay in L2 throughout.
 // LayerNorm is a row-wise pass (one warp per row) over the staged pre-norm rows.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -47,10 +47,6 @@ constexpr int kGemmThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KB
 
-constexpr int kCluster = 2;                  // CTAs sharing a B tile
-constexpr uint16_t kClusterMask = 0x3;
-constexpr uint32_t kBHalfBytes = kBBytes / kCluster;
-
 struct GemmSmem {  // placed at a 1024-byte aligned address
   uint8_t a[kStages][kABytes];
   uint8_t b[kStages][kBBytes];
@@ -69,39 +65,6 @@ struct GemmParams {
   int32_t* status;
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Both CTAs of the cluster: barrier over every thread (release / acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Tiled 2-D TMA load whose data and byte count land at the same shared-memory offsets (buffer
-// and mbarrier) in every CTA of `mask` within this cluster.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map,
-                                                      int c0, int c1, uint64_t* bar,
-                                                      uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-
-// Arrive (once) on the mbarrier at `bar`'s offset in every CTA of `mask` when all tcgen05
-// operations this thread issued so far have completed.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int32_t* status) {
   if (mbar_wait_bounded(bar, parity)) return true;
   flag_error(status, PA_DEV_ERR_TIMEOUT);
@@ -116,17 +79,15 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
   GemmSmem& s = *reinterpret_cast<GemmSmem*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (p.M + kBM - 1) / kBM, n_tiles = p.N / kBN;
-  // a unit is a pair of row tiles (2i, 2i + 1) x one column tile; this CTA takes row tile
-  // 2i + rank (past the last row tile it loads zeros and stores nothing)
-  const int units = ((m_tiles + 1) / 2) * n_tiles;
+  // unit u = row tile u / n_tiles x column tile u % n_tiles; CTA c takes units c, c + G, ...
+  const int units = m_tiles * n_tiles;
   const int k_blocks = p.K / kBK;
-  const int rank = static_cast<int>(cluster_rank());
-  const int cl = static_cast<int>(blockIdx.x) / kCluster, n_cl = static_cast<int>(gridDim.x) / kCluster;
+  const int cl = static_cast<int>(blockIdx.x), n_cl = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], kCluster);   // one commit from each CTA's MMA issuer
+      mbar_init(&s.empty[i], 1);   // the MMA issuer's commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.acc_full[i], 1);
@@ -137,7 +98,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
   }
   if (warp == 5) tc::tmem_alloc<512>(&s.tmem_base);
   tc::fence_before_sync();
-  cluster_sync();   // the peer's barriers exist before anything is multicast into them
+  __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
 
@@ -147,16 +108,14 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
       uint32_t it = 0;
       bool ok = true;
       for (int u = cl; u < units && ok; u += n_cl) {
-        const int m0 = (2 * (u / n_tiles) + rank) * kBM, n0 = (u % n_tiles) * kBN;
+        const int m0 = (u / n_tiles) * kBM, n0 = (u % n_tiles) * kBN;
         for (int kb = 0; kb < k_blocks && ok; ++kb, ++it) {
           const int st = it % kStages;
-          // both CTAs' MMAs have released this stage, so both may now receive data
           ok = wait_or_flag(&s.empty[st], ((it / kStages) & 1) ^ 1u, p.status);
           if (!ok) break;
           mbar_arrive_expect_tx(&s.full[st], kABytes + kBBytes);
           tc::tma_load_2d(s.a[st], &a_map, kb * kBK, m0, &s.full[st]);
-          tma_load_2d_multicast(s.b[st] + rank * kBHalfBytes, &b_map, kb * kBK,
-                                n0 + rank * (kBN / kCluster), &s.full[st], kClusterMask);
+          tc::tma_load_2d(s.b[st], &b_map, kb * kBK, n0, &s.full[st]);
         }
       }
       // do not leave while copies into shared memory may still be landing
@@ -186,7 +145,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
             tc::mma_ss(tmem + acc * kBN, tc::smem_desc_sw128(aa + kk * 32, 16, 1024),
                        tc::smem_desc_sw128(bb + kk * 32, 16, 1024), idesc,
                        (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_multicast(&s.empty[st], kClusterMask);
+          tc::mma_commit(&s.empty[st]);
         }
         if (ok) tc::mma_commit(&s.acc_full[acc]);
       }
@@ -204,7 +163,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
       if (!__all_sync(0xffffffffu, wait_or_flag(&s.acc_full[acc], (tc_n >> 1) & 1, p.status)))
         break;
       tc::fence_after_sync();
-      const int m0 = (2 * (u / n_tiles) + rank) * kBM, n0 = (u % n_tiles) * kBN;
+      const int m0 = (u / n_tiles) * kBM, n0 = (u % n_tiles) * kBN;
       const int row = m0 + r;
       uint16_t* dst = p.c + static_cast<int64_t>(row) * p.N + n0;
 #pragma unroll 1
@@ -242,8 +201,7 @@ gemm_bias_act_kernel(const __grid_constant__ CUtensorMap a_map,
   }
 
   tc::fence_before_sync();
-  // the peer may still multicast into this CTA or arrive on its barriers until it is done too
-  cluster_sync();
+  __syncthreads();
   if (warp == 5) {
     tc::fence_after_sync();
     tc::tmem_dealloc<512>(tmem);
@@ -310,7 +268,7 @@ pa_status launch_gemm(const void* a, int64_t lda_bytes, const void* b, int M, in
   if (!make_map_2d(&am, a, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
                    static_cast<uint64_t>(lda_bytes), kBM) ||
       !make_map_2d(&bm, b, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                   static_cast<uint64_t>(K) * 2, kBN / kCluster)) {
+                   static_cast<uint64_t>(K) * 2, kBN)) {
     snprintf_error("cuTensorMapEncodeTiled failed for the adaptor operands");
     return PA_ERR_CUDA;
   }
@@ -325,22 +283,11 @@ pa_status launch_gemm(const void* a, int64_t lda_bytes, const void* b, int M, in
     configured_device = dev;
   }
   const int sms = sm_count_current_device();
-  if (sms < kCluster) return PA_ERR_CUDA;
+  if (sms <= 0) return PA_ERR_CUDA;
   GemmParams p{M, N, K, bias, static_cast<uint16_t*>(c), silu ? 1 : 0, status};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sms / kCluster * kCluster);   // one CTA per SM, in pairs
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bias_act_kernel, am, bm, p);
-  if (e != cudaSuccess) return record_cuda_error(e, "gemm_bias_act_kernel");
+  const int units = (M + kBM - 1) / kBM * (N / kBN);
+  gemm_bias_act_kernel<<<std::min(sms, units), kGemmThreads, smem, stream>>>(am, bm, p);  // one CTA per SM
+  PA_CHECK_LAUNCH("gemm_bias_act_kernel");
   return PA_OK;
 }
 

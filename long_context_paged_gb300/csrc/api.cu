@@ -68,4 +68,4 @@ extern "C" const char* pa_status_string(pa_status s) {
 
 extern "C" const char* pa_last_error(void) { return pa::g_last_error; }
 
-extern "C" int32_t pa_version(void) { return 100; }
+extern "C" int32_t pa_version(void) { return 200; }

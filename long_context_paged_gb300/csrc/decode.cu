@@ -8,9 +8,11 @@
 //
 // Design (GB300):
 //  * Persistent grid, one CTA per SM. The pages of all sequences are laid end to end and cut
-//    into equal contiguous page ranges, one per CTA, so a ragged batch (375 .. 70,000 tokens)
-//    is balanced to within one page. A sequence cut by a range boundary yields one partial
-//    (o, lse) per CTA that touches it; a second small kernel merges them by log-sum-exp.
+//    into contiguous page ranges: by default one equal range per CTA, so a ragged batch
+//    (375 .. 70,000 tokens) is balanced to within one page; with an explicit split size the
+//    ranges are that many pages and CTA c takes ranges c, c + G, ... A sequence cut by a range
+//    boundary yields one partial (o, lse) per range that touches it; a second small kernel
+//    merges them by log-sum-exp.
 //  * A page holds 16 tokens x 8 KV heads x 128 dims of K (32 KB, contiguous) and the same of
 //    V. A producer warp streams whole pages into a 3-stage shared-memory ring with bulk
 //    asynchronous copies (cp.async.bulk + mbarrier transaction counts): 64 KB per stage,
@@ -65,14 +67,18 @@ struct DecodeParams {
   const int32_t* seq_lens;
   int32_t batch;
   int32_t max_seq_len;
+  int32_t split_pages;  // pages per range; 0 = an equal share per CTA
+  int32_t max_ranges;   // ranges the workspace has records for (the grid size by default)
   float scale_log2;
   uint16_t* out;
   float* lse;
-  int32_t* ws_header;  // [0] = pages per CTA (W), [1] = total pages, [2] = grid size
+  int32_t* ws_header;  // [0] = pages per range (W), [1] = total pages, [2] = grid size
   int32_t* ws_prefix;  // [batch + 1]
   float* ws_lse;       // [records][Hq]
   float* ws_o;         // [records][Hq][D]
   int32_t* status;
+  uint64_t wait_limit_ns;  // bound of every mbarrier wait
+  int32_t starve;          // test hook: CTA 0 never fills its first ring stage
 };
 
 // Keys of sequence b as the kernels use them: negative -> 0, more than the table row covers
@@ -150,10 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
   build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
 
   const int total = s.total;
-  // pages per CTA: an equal share (at least kMinPagesPerCta). A short batch is spread over as
-  // many SMs as it has pages: one SM ingests a 32 KB page in well under a microsecond, so a
+  // pages per range: an equal share per CTA (at least kMinPagesPerCta) unless a split size was
+  // given; never fewer than the workspace has records for. A short batch is spread over as many
+  // SMs as it has pages: one SM ingests a 32 KB page in well under a microsecond, so a
   // single-sequence decode is latency-bound, and its partials merge in parallel per head.
-  const int W = max((total + gridDim.x - 1) / gridDim.x, kMinPagesPerCta);
+  const int base = p.split_pages > 0 ? p.split_pages : kMinPagesPerCta;
+  const int W = max((total + p.max_ranges - 1) / p.max_ranges, base);
   if (blockIdx.x == 0) {
     if (tid == 0) {
       p.ws_header[0] = W;
@@ -163,10 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
     for (int b = tid; b <= p.batch; b += kThreads) p.ws_prefix[b] = s.prefix[b];
   }
   if (total == 0) return;
-  const int P0 = blockIdx.x * W;
-  const int P1 = min(total, P0 + W);
-  if (P0 >= P1) return;
-  const int b_first = find_seq(s.prefix, p.batch, P0);
+  const int n_ranges = (total + W - 1) / W;  // <= max_ranges
+  if (static_cast<int>(blockIdx.x) >= n_ranges) return;
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
@@ -174,48 +180,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
     uint32_t phase = 0;
     int issued = 0;
     bool ok = true;
-    for (int b = b_first; ok && b < p.batch && s.prefix[b] < P1; ++b) {
-      const int lp0 = max(P0, s.prefix[b]) - s.prefix[b];
-      const int lp1 = min(P1, s.prefix[b + 1]) - s.prefix[b];
-      const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-      for (int lp = lp0; ok && lp < lp1; lp += 32) {
-        const int n = min(32, lp1 - lp);
-        int entry = 0;
-        if (lane < n) {
-          entry = bt_row[lp + lane];
-          if (entry < 0 || entry >= p.num_pages) {
-            flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
-            entry = 0;
-          }
-        }
-        for (int i = 0; i < n; ++i) {
-          const int page = __shfl_sync(0xffffffffu, entry, i);
-          if (lane == 0) {
-            if (!mbar_wait_bounded(&s.empty[stage], phase ^ 1u)) {
-              flag_error(p.status, PA_DEV_ERR_TIMEOUT);
-              ok = false;
-            } else {
-              mbar_arrive_expect_tx(&s.full[stage], 2 * kPageBytes);
-              bulk_g2s(s.kv[stage][0], p.k_pool + static_cast<int64_t>(page) * kPageBytes,
-                       kPageBytes, &s.full[stage]);
-              bulk_g2s(s.kv[stage][1], p.v_pool + static_cast<int64_t>(page) * kPageBytes,
-                       kPageBytes, &s.full[stage]);
-              ++issued;
+    bool starve = p.starve != 0 && blockIdx.x == 0;
+    for (int rg = blockIdx.x; ok && rg < n_ranges; rg += gridDim.x) {
+      const int P0 = rg * W, P1 = min(total, P0 + W);
+      const int b_first = find_seq(s.prefix, p.batch, P0);
+      for (int b = b_first; ok && b < p.batch && s.prefix[b] < P1; ++b) {
+        const int lp0 = max(P0, s.prefix[b]) - s.prefix[b];
+        const int lp1 = min(P1, s.prefix[b + 1]) - s.prefix[b];
+        const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+        for (int lp = lp0; ok && lp < lp1; lp += 32) {
+          const int n = min(32, lp1 - lp);
+          int entry = 0;
+          if (lane < n) {
+            entry = bt_row[lp + lane];
+            if (entry < 0 || entry >= p.num_pages) {
+              flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
+              entry = 0;
             }
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          for (int i = 0; i < n; ++i) {
+            const int page = __shfl_sync(0xffffffffu, entry, i);
+            if (lane == 0) {
+              if (starve) {
+                starve = false;  // this stage stays empty: its consumers' waits run out
+              } else if (!mbar_wait_bounded(&s.empty[stage], phase ^ 1u, p.wait_limit_ns)) {
+                flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+                ok = false;
+              } else {
+                mbar_arrive_expect_tx(&s.full[stage], 2 * kPageBytes);
+                bulk_g2s(s.kv[stage][0], p.k_pool + static_cast<int64_t>(page) * kPageBytes,
+                         kPageBytes, &s.full[stage]);
+                bulk_g2s(s.kv[stage][1], p.v_pool + static_cast<int64_t>(page) * kPageBytes,
+                         kPageBytes, &s.full[stage]);
+                ++issued;
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          }
         }
       }
     }
-    // Do not leave while copies into this CTA's shared memory may still be landing.
+    // Do not leave while copies into this CTA's shared memory may still be landing (the last
+    // `issued` ring positions; a stage left empty by the test hook is the first one, never
+    // among them).
     if (lane == 0) {
       int st = stage;
       uint32_t ph = phase;
       for (int k = 0; k < min(issued, kStages); ++k) {
         if (--st < 0) { st = kStages - 1; ph ^= 1u; }
-        if (!mbar_wait_bounded(&s.full[st], ph)) flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+        if (!mbar_wait_bounded(&s.full[st], ph, p.wait_limit_ns)) flag_error(p.status, PA_DEV_ERR_TIMEOUT);
       }
     }
     return;
@@ -229,178 +244,182 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
   int stage = 0;
   uint32_t phase = 0;
 
-  for (int b = b_first; b < p.batch && s.prefix[b] < P1; ++b) {
-    const int n_pages = s.prefix[b + 1] - s.prefix[b];
-    const int lp0 = max(P0, s.prefix[b]) - s.prefix[b];
-    const int lp1 = min(P1, s.prefix[b + 1]) - s.prefix[b];
-    if (lp0 >= lp1) continue;
-    const int L = clamp_len(p, b, false);
+  for (int rg = blockIdx.x; rg < n_ranges; rg += gridDim.x) {
+    const int P0 = rg * W, P1 = min(total, P0 + W);
+    const int b_first = find_seq(s.prefix, p.batch, P0);
+    for (int b = b_first; b < p.batch && s.prefix[b] < P1; ++b) {
+      const int n_pages = s.prefix[b + 1] - s.prefix[b];
+      const int lp0 = max(P0, s.prefix[b]) - s.prefix[b];
+      const int lp1 = min(P1, s.prefix[b + 1]) - s.prefix[b];
+      if (lp0 >= lp1) continue;
+      const int L = clamp_len(p, b, false);
 
-    float2 qa[4], qb[4];
-    {
-      const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHq + 2 * g) * kHeadDim + 8 * c;
-      const uint4 ra = *reinterpret_cast<const uint4*>(qrow);
-      const uint4 rb = *reinterpret_cast<const uint4*>(qrow + kHeadDim);
-      const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qa[i] = make_float2(bf16lo(wa[i]) * p.scale_log2, bf16hi(wa[i]) * p.scale_log2);
-        qb[i] = make_float2(bf16lo(wb[i]) * p.scale_log2, bf16hi(wb[i]) * p.scale_log2);
-      }
-    }
-    float2 acc_a[4], acc_b[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc_a[i] = acc_b[i] = make_float2(0.f, 0.f);
-    float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F;  // max used for the exponent, per head
-    float l_part = 0.f;                               // this lane's share of its head's sum
-
-    bool all_ok = true;
-    for (int lp = lp0; lp < lp1; ++lp) {
-      const int n_valid = min(kPage, L - lp * kPage);
-      bool ok = true;
-      if (!mbar_wait_bounded(&s.full[stage], phase)) {
-        flag_error(p.status, PA_DEV_ERR_TIMEOUT);
-        ok = false;
-      }
-      if (!__all_sync(0xffffffffu, ok)) {
-        all_ok = false;
-        break;
-      }
-      const uint8_t* Ks = s.kv[stage][0] + g * (kHeadDim * 2) + c * 16;
-      const uint8_t* Vs = s.kv[stage][1] + g * (kHeadDim * 2) + c * 16;
-
-      // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 kr = lds128(Ks + (th * 8 + j) * (kHkv * kHeadDim * 2));
-        const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
-        const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
-        const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
-        const float2 k3 = make_float2(bf16lo(kr.w), bf16hi(kr.w));
-        float2 sa = mul2(qa[0], k0), sb = mul2(qb[0], k0);
-        sa = fma2(qa[1], k1, sa); sb = fma2(qb[1], k1, sb);
-        sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
-        sa = fma2(qa[3], k3, sa); sb = fma2(qb[3], k3, sb);
-        v[j] = sa.x + sa.y;
-        v[8 + j] = sb.x + sb.y;
-      }
-      // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score
-      //      of token th*8 + (c & 7), head (c >> 3).
-#pragma unroll
-      for (int w = 8; w >= 1; w >>= 1) {
-        const bool up = (c & w) != 0;
-#pragma unroll
-        for (int i = 0; i < w; ++i) {
-          const float send = up ? v[i] : v[w + i];
-          const float keep = up ? v[w + i] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
-      }
-      float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
-
-      // ---- page max per head, lazily moved running max
-      float pm = sc;
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-      const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
-      const float pmax_a = hi_head ? pm_other : pm;
-      const float pmax_b = hi_head ? pm : pm_other;
-      if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
-        const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
-        const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
-        const float al_b = (m_b == -CUDART_INF_F) ? 0.f : fast_exp2(m_b - nb);
-        const float2 fa = make_float2(al_a, al_a), fb = make_float2(al_b, al_b);
+      float2 qa[4], qb[4];
+      {
+        const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHq + 2 * g) * kHeadDim + 8 * c;
+        const uint4 ra = *reinterpret_cast<const uint4*>(qrow);
+        const uint4 rb = *reinterpret_cast<const uint4*>(qrow + kHeadDim);
+        const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          acc_a[i] = mul2(acc_a[i], fa);
-          acc_b[i] = mul2(acc_b[i], fb);
-        }
-        l_part *= hi_head ? al_b : al_a;
-        m_a = na;
-        m_b = nb;
-      }
-      const float pr = fast_exp2(sc - (hi_head ? m_b : m_a));
-      l_part += pr;
-
-      // ---- hand probabilities to the lanes that own the V dims
-      s.p[warp][lane] = pr;
-      __syncwarp();
-      const float4 pa0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 0]);
-      const float4 pa1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 4]);
-      const float4 pb0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 8]);
-      const float4 pb1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 12]);
-      const float pav[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
-      const float pbv[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
-
-      // ---- o += p v over this lane's 8 tokens (invalid slots of a partial page skipped)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (th * 8 + j < n_valid) {
-          const uint4 vr = lds128(Vs + (th * 8 + j) * (kHkv * kHeadDim * 2));
-          const float2 ppa = make_float2(pav[j], pav[j]);
-          const float2 ppb = make_float2(pbv[j], pbv[j]);
-          const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
-          const float2 v1 = make_float2(bf16lo(vr.y), bf16hi(vr.y));
-          const float2 v2 = make_float2(bf16lo(vr.z), bf16hi(vr.z));
-          const float2 v3 = make_float2(bf16lo(vr.w), bf16hi(vr.w));
-          acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
-          acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
-          acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
-          acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
+          qa[i] = make_float2(bf16lo(wa[i]) * p.scale_log2, bf16hi(wa[i]) * p.scale_log2);
+          qb[i] = make_float2(bf16lo(wb[i]) * p.scale_log2, bf16hi(wb[i]) * p.scale_log2);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.empty[stage]);
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
-    }
-    if (!all_ok) return;
+      float2 acc_a[4], acc_b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc_a[i] = acc_b[i] = make_float2(0.f, 0.f);
+      float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F;  // max used for the exponent, per head
+      float l_part = 0.f;                               // this lane's share of its head's sum
 
-    // ---- finish this (sequence, range): denominators and the two token halves
-    float l_m = l_part;
-    l_m += __shfl_xor_sync(0xffffffffu, l_m, 1);
-    l_m += __shfl_xor_sync(0xffffffffu, l_m, 2);
-    l_m += __shfl_xor_sync(0xffffffffu, l_m, 4);
-    l_m += __shfl_xor_sync(0xffffffffu, l_m, 16);
-    const float l_o = __shfl_xor_sync(0xffffffffu, l_m, 8);
-    const float l_a = hi_head ? l_o : l_m;
-    const float l_b = hi_head ? l_m : l_o;
+      bool all_ok = true;
+      for (int lp = lp0; lp < lp1; ++lp) {
+        const int n_valid = min(kPage, L - lp * kPage);
+        bool ok = true;
+        if (!mbar_wait_bounded(&s.full[stage], phase, p.wait_limit_ns)) {
+          flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+          ok = false;
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          all_ok = false;
+          break;
+        }
+        const uint8_t* Ks = s.kv[stage][0] + g * (kHeadDim * 2) + c * 16;
+        const uint8_t* Vs = s.kv[stage][1] + g * (kHeadDim * 2) + c * 16;
+
+        // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
+        float v[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc_a[i].x += __shfl_xor_sync(0xffffffffu, acc_a[i].x, 16);
-      acc_a[i].y += __shfl_xor_sync(0xffffffffu, acc_a[i].y, 16);
-      acc_b[i].x += __shfl_xor_sync(0xffffffffu, acc_b[i].x, 16);
-      acc_b[i].y += __shfl_xor_sync(0xffffffffu, acc_b[i].y, 16);
-    }
-    // lanes 0..15 finish head 2g, lanes 16..31 head 2g+1
-    const int head = 2 * g + th;
-    const float l_h = th ? l_b : l_a;
-    const float m_h = th ? m_b : m_a;
-    const float inv = 1.0f / l_h;
-    float o[8];
+        for (int j = 0; j < 8; ++j) {
+          const uint4 kr = lds128(Ks + (th * 8 + j) * (kHkv * kHeadDim * 2));
+          const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
+          const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
+          const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
+          const float2 k3 = make_float2(bf16lo(kr.w), bf16hi(kr.w));
+          float2 sa = mul2(qa[0], k0), sb = mul2(qb[0], k0);
+          sa = fma2(qa[1], k1, sa); sb = fma2(qb[1], k1, sb);
+          sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
+          sa = fma2(qa[3], k3, sa); sb = fma2(qb[3], k3, sb);
+          v[j] = sa.x + sa.y;
+          v[8 + j] = sb.x + sb.y;
+        }
+        // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score
+        //      of token th*8 + (c & 7), head (c >> 3).
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 a = th ? acc_b[i] : acc_a[i];
-      o[2 * i] = a.x * inv;
-      o[2 * i + 1] = a.y * inv;
-    }
-    const float lse_h = (m_h + log2f(l_h)) * kLn2;
-    if (lp0 == 0 && lp1 == n_pages) {
-      uint4 w;
-      w.x = pack_bf16x2(o[0], o[1]);
-      w.y = pack_bf16x2(o[2], o[3]);
-      w.z = pack_bf16x2(o[4], o[5]);
-      w.w = pack_bf16x2(o[6], o[7]);
-      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + head) * kHeadDim + 8 * c) = w;
-      if (c == 0 && p.lse != nullptr) p.lse[b * kHq + head] = lse_h;
-    } else {
-      const int64_t r = static_cast<int64_t>(b) + blockIdx.x;
-      float* dst = p.ws_o + (r * kHq + head) * kHeadDim + 8 * c;
-      reinterpret_cast<float4*>(dst)[0] = make_float4(o[0], o[1], o[2], o[3]);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(o[4], o[5], o[6], o[7]);
-      if (c == 0) p.ws_lse[r * kHq + head] = lse_h;
+        for (int w = 8; w >= 1; w >>= 1) {
+          const bool up = (c & w) != 0;
+#pragma unroll
+          for (int i = 0; i < w; ++i) {
+            const float send = up ? v[i] : v[w + i];
+            const float keep = up ? v[w + i] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+          }
+        }
+        float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
+
+        // ---- page max per head, lazily moved running max
+        float pm = sc;
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+        const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
+        const float pmax_a = hi_head ? pm_other : pm;
+        const float pmax_b = hi_head ? pm : pm_other;
+        if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
+          const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
+          const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
+          const float al_b = (m_b == -CUDART_INF_F) ? 0.f : fast_exp2(m_b - nb);
+          const float2 fa = make_float2(al_a, al_a), fb = make_float2(al_b, al_b);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc_a[i] = mul2(acc_a[i], fa);
+            acc_b[i] = mul2(acc_b[i], fb);
+          }
+          l_part *= hi_head ? al_b : al_a;
+          m_a = na;
+          m_b = nb;
+        }
+        const float pr = fast_exp2(sc - (hi_head ? m_b : m_a));
+        l_part += pr;
+
+        // ---- hand probabilities to the lanes that own the V dims
+        s.p[warp][lane] = pr;
+        __syncwarp();
+        const float4 pa0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 0]);
+        const float4 pa1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 4]);
+        const float4 pb0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 8]);
+        const float4 pb1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 12]);
+        const float pav[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
+        const float pbv[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
+
+        // ---- o += p v over this lane's 8 tokens (invalid slots of a partial page skipped)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (th * 8 + j < n_valid) {
+            const uint4 vr = lds128(Vs + (th * 8 + j) * (kHkv * kHeadDim * 2));
+            const float2 ppa = make_float2(pav[j], pav[j]);
+            const float2 ppb = make_float2(pbv[j], pbv[j]);
+            const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
+            const float2 v1 = make_float2(bf16lo(vr.y), bf16hi(vr.y));
+            const float2 v2 = make_float2(bf16lo(vr.z), bf16hi(vr.z));
+            const float2 v3 = make_float2(bf16lo(vr.w), bf16hi(vr.w));
+            acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
+            acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
+            acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
+            acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!all_ok) return;
+
+      // ---- finish this (sequence, range): denominators and the two token halves
+      float l_m = l_part;
+      l_m += __shfl_xor_sync(0xffffffffu, l_m, 1);
+      l_m += __shfl_xor_sync(0xffffffffu, l_m, 2);
+      l_m += __shfl_xor_sync(0xffffffffu, l_m, 4);
+      l_m += __shfl_xor_sync(0xffffffffu, l_m, 16);
+      const float l_o = __shfl_xor_sync(0xffffffffu, l_m, 8);
+      const float l_a = hi_head ? l_o : l_m;
+      const float l_b = hi_head ? l_m : l_o;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc_a[i].x += __shfl_xor_sync(0xffffffffu, acc_a[i].x, 16);
+        acc_a[i].y += __shfl_xor_sync(0xffffffffu, acc_a[i].y, 16);
+        acc_b[i].x += __shfl_xor_sync(0xffffffffu, acc_b[i].x, 16);
+        acc_b[i].y += __shfl_xor_sync(0xffffffffu, acc_b[i].y, 16);
+      }
+      // lanes 0..15 finish head 2g, lanes 16..31 head 2g+1
+      const int head = 2 * g + th;
+      const float l_h = th ? l_b : l_a;
+      const float m_h = th ? m_b : m_a;
+      const float inv = 1.0f / l_h;
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = th ? acc_b[i] : acc_a[i];
+        o[2 * i] = a.x * inv;
+        o[2 * i + 1] = a.y * inv;
+      }
+      const float lse_h = (m_h + log2f(l_h)) * kLn2;
+      if (lp0 == 0 && lp1 == n_pages) {
+        uint4 w;
+        w.x = pack_bf16x2(o[0], o[1]);
+        w.y = pack_bf16x2(o[2], o[3]);
+        w.z = pack_bf16x2(o[4], o[5]);
+        w.w = pack_bf16x2(o[6], o[7]);
+        *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + head) * kHeadDim + 8 * c) = w;
+        if (c == 0 && p.lse != nullptr) p.lse[b * kHq + head] = lse_h;
+      } else {
+        const int64_t r = static_cast<int64_t>(b) + rg;  // unique per (sequence, range)
+        float* dst = p.ws_o + (r * kHq + head) * kHeadDim + 8 * c;
+        reinterpret_cast<float4*>(dst)[0] = make_float4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(o[4], o[5], o[6], o[7]);
+        if (c == 0) p.ws_lse[r * kHq + head] = lse_h;
+      }
     }
   }
 }
@@ -496,9 +515,9 @@ struct WsLayout {
   size_t header, prefix, lse, o, total;
 };
 
-WsLayout ws_layout(int batch, int grid) {
+WsLayout ws_layout(int batch, int64_t ranges) {
   WsLayout w;
-  const size_t records = static_cast<size_t>(batch) + grid;
+  const size_t records = static_cast<size_t>(batch) + static_cast<size_t>(ranges);
   w.header = 0;
   w.prefix = 256;
   w.lse = align_up(w.prefix + sizeof(int32_t) * (batch + 1), 256);
@@ -512,32 +531,78 @@ bool dims_supported(const pa_dims& d) {
          d.page_size == kPage;
 }
 
+// With an explicit split size, at most this many ranges per SM (the split is raised beyond
+// that, which bounds the workspace: 64 ranges x 152 SMs x 8 KB of partials = 80 MB).
+constexpr int64_t kMaxRangesPerSm = 64;
+
+// Launch plan of one call, from host arguments only (so that it can be captured in a graph).
+struct DecodePlan {
+  int grid;          // CTAs
+  int split_pages;   // 0 = an equal share per CTA
+  int max_ranges;    // ranges of the launch (records = batch + max_ranges)
+  int64_t ws_ranges; // ranges the workspace must hold records for
+};
+
+DecodePlan decode_plan(int batch, int max_seq_len, int split_tokens, int sm_grid) {
+  DecodePlan d;
+  // pages the batch can have at most
+  const int64_t page_bound = std::max<int64_t>(
+      1, static_cast<int64_t>(batch) * ((static_cast<int64_t>(max_seq_len) + kPage - 1) / kPage));
+  if (split_tokens == 0) {
+    // one CTA per SM, but no more CTAs than the batch can have pages (a short batch then
+    // launches only the CTAs that get work); the workspace size does not depend on max_seq_len
+    d.grid = static_cast<int>(std::min<int64_t>(sm_grid, page_bound));
+    d.split_pages = 0;
+    d.max_ranges = d.grid;
+    d.ws_ranges = sm_grid;
+  } else {
+    const int64_t pages = (static_cast<int64_t>(split_tokens) + kPage - 1) / kPage;
+    const int64_t ranges = std::min<int64_t>((page_bound + pages - 1) / pages, kMaxRangesPerSm * sm_grid);
+    d.split_pages = static_cast<int>(pages);
+    d.max_ranges = static_cast<int>(ranges);
+    d.grid = static_cast<int>(std::min<int64_t>(sm_grid, ranges));
+    d.ws_ranges = ranges;
+  }
+  return d;
+}
+
+// Test hook (pa_debug_decode_starve): the calling thread's next launches leave one ring stage
+// of CTA 0 empty and bound every wait by 1 ms.
+thread_local bool g_debug_starve = false;
+constexpr uint64_t kDebugWaitLimitNs = 1000000ull;
+
 }  // namespace
 
 int decode_grid_size() { return sm_count_current_device(); }
 
 }  // namespace pa
 
-extern "C" size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len) {
-  (void)max_seq_len;
-  if (batch < 0) return 0;
+extern "C" size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len,
+                                           int32_t split_tokens) {
   (void)dims;
-  const int grid = pa::decode_grid_size();
-  if (grid <= 0) return 0;
-  return pa::ws_layout(batch, grid).total;
+  if (batch < 0 || max_seq_len < 0 || split_tokens < 0) return 0;
+  const int sm_grid = pa::decode_grid_size();
+  if (sm_grid <= 0) return 0;
+  return pa::ws_layout(batch, pa::decode_plan(batch, max_seq_len, split_tokens, sm_grid).ws_ranges).total;
+}
+
+extern "C" pa_status pa_debug_decode_starve(int32_t enable) {
+  pa::g_debug_starve = enable != 0;
+  return PA_OK;
 }
 
 extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool,
                                        const void* v_pool, int64_t num_pages,
                                        const int32_t* block_table, int32_t bt_stride,
                                        const int32_t* seq_lens, int32_t batch,
-                                       int32_t max_seq_len, float softmax_scale, void* out,
-                                       float* lse, void* workspace, size_t workspace_bytes,
-                                       int32_t* status, pa_stream_t stream) {
+                                       int32_t max_seq_len, float softmax_scale,
+                                       int32_t split_tokens, void* out, float* lse,
+                                       void* workspace, size_t workspace_bytes, int32_t* status,
+                                       pa_stream_t stream) {
   using namespace pa;
   if (!dims_supported(dims)) return PA_ERR_UNSUPPORTED;
   if (batch < 0 || batch > kMaxBatch || bt_stride <= 0 || num_pages <= 0 || max_seq_len < 0 ||
-      max_seq_len > 131072 || !(softmax_scale == softmax_scale))
+      max_seq_len > 131072 || !(softmax_scale == softmax_scale) || split_tokens < 0)
     return PA_ERR_INVALID_ARG;
   if (batch == 0) return PA_OK;
   if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !workspace)
@@ -548,13 +613,9 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
   const int sm_grid = decode_grid_size();
   if (sm_grid <= 0) return PA_ERR_CUDA;
-  if (workspace_bytes < ws_layout(batch, sm_grid).total) return PA_ERR_WORKSPACE_TOO_SMALL;
-  // one CTA per SM, but no more CTAs than the batch can have pages (a short batch then
-  // launches only the CTAs that get work)
-  const int64_t page_bound =
-      static_cast<int64_t>(batch) * ((static_cast<int64_t>(max_seq_len) + kPage - 1) / kPage);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sm_grid, page_bound)));
-  const WsLayout w = ws_layout(batch, grid);
+  const DecodePlan plan = decode_plan(batch, max_seq_len, split_tokens, sm_grid);
+  if (workspace_bytes < ws_layout(batch, plan.ws_ranges).total) return PA_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout w = ws_layout(batch, plan.max_ranges);
 
   static thread_local int configured_device = -1;
   int dev = 0;
@@ -587,6 +648,8 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   p.seq_lens = seq_lens;
   p.batch = batch;
   p.max_seq_len = max_seq_len;
+  p.split_pages = plan.split_pages;
+  p.max_ranges = plan.max_ranges;
   p.scale_log2 = softmax_scale * kLog2e;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
@@ -596,15 +659,17 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   p.ws_lse = reinterpret_cast<float*>(ws + w.lse);
   p.ws_o = reinterpret_cast<float*>(ws + w.o);
   p.status = status;
+  p.wait_limit_ns = g_debug_starve ? kDebugWaitLimitNs : kWaitLimitNs;
+  p.starve = g_debug_starve ? 1 : 0;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  decode_splitkv_kernel<<<grid, kThreads, sizeof(DecodeSmem), st>>>(p);
+  decode_splitkv_kernel<<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p);
   PA_CHECK_LAUNCH("decode_splitkv_kernel");
   {
     cudaLaunchConfig_t cfg = {};
-    // partials per sequence when the lengths are equal: ceil(grid / batch), plus one for a cut
-    // at each end; more than 4 warps take in one round of 4 loads -> 16 warps per head
-    const bool small = (grid + batch - 1) / batch + 1 > 4 * kMergeWarpsLarge;
+    // partials per sequence when the lengths are equal: ceil(ranges / batch), plus one for a
+    // cut at each end; more than 4 warps take in one round of 4 loads -> 16 warps per head
+    const bool small = (plan.max_ranges + batch - 1) / batch + 1 > 4 * kMergeWarpsLarge;
     cfg.gridDim = dim3(batch, kHq);
     cfg.blockDim = dim3((small ? kMergeWarpsSmall : kMergeWarpsLarge) * 32);
     cfg.dynamicSmemBytes = 0;
@@ -674,7 +739,7 @@ extern "C" pa_status attn_decode_paged_noalloc(pa_dims dims, const void* q, cons
   if (batch > 0) {
     const int grid = decode_grid_size();
     if (grid <= 0) return PA_ERR_CUDA;
-    const size_t need = ws_layout(batch, grid).total;
+    const size_t need = ws_layout(batch, decode_plan(batch, max_seq_len, 0, grid).ws_ranges).total;
     if (need > kStaticScratchBytes) {
       snprintf_error("attn_decode_paged_noalloc: batch %d needs %zu bytes of scratch on this GPU, "
                      "more than the built-in %zu bytes; use attn_decode_paged with a workspace",
@@ -686,6 +751,6 @@ extern "C" pa_status attn_decode_paged_noalloc(pa_dims dims, const void* q, cons
   const pa_status st = static_scratch(&scratch);
   if (st != PA_OK) return st;
   return attn_decode_paged(dims, q, k_pool, v_pool, num_pages, block_table, bt_stride, seq_lens,
-                           batch, max_seq_len, softmax_scale, out, lse, scratch,
+                           batch, max_seq_len, softmax_scale, 0, out, lse, scratch,
                            kStaticScratchBytes, status, stream);
 }

@@ -33,7 +33,11 @@ struct AppendParams {
 
 __global__ void __launch_bounds__(2 * kRowChunks) kv_append_kernel(const AppendParams p) {
   const int t = blockIdx.x;
-  if (t >= p.cu_new_lens[p.batch]) return;  // rows past the packed total are not tokens
+  const int packed = p.cu_new_lens[p.batch];
+  // more packed rows than the call's total_new: the rows past it would be lost silently
+  if (t == 0 && threadIdx.x == 0 && packed > static_cast<int>(gridDim.x))
+    flag_error(p.status, PA_DEV_ERR_LENGTH);
+  if (t >= packed) return;  // rows past the packed total are not tokens
   int lo = 0, hi = p.batch;                  // largest b with cu[b] <= t
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;

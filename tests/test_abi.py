@@ -53,25 +53,25 @@ def test_argument_errors_are_rejected_before_launch(lib):
     good = pa.Dims(*pa.DEFAULT_DIMS)
     null = None
     # unsupported shape
-    assert lib.attn_decode_paged(bad_dims, null, null, null, 1, null, 1, null, 1, 16, 1.0,
+    assert lib.attn_decode_paged(bad_dims, null, null, null, 1, null, 1, null, 1, 16, 1.0, 0,
                                  null, null, null, 0, null, null) == 2
     assert lib.attn_prefill_chunk(pa.Dims(16, 4, 128, 16), null, null, 1, null, null, 1, null, 1,
                                   null, 1, 1, 16, 1.0, null, null, null, 0, null, null) == 2
     assert lib.kv_append_paged(pa.Dims(16, 8, 128, 32), null, null, 1, null, null, 1, null, 1,
                                null, null, 1, null, null) == 2
     # negative sizes / null pointers
-    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, -1, 16, 1.0,
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, -1, 16, 1.0, 0,
                                  null, null, null, 0, null, null) == 1
-    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 2, 16, 1.0,
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 2, 16, 1.0, 0,
                                  null, null, null, 0, null, null) == 1
-    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 1, 200000, 1.0,
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 1, 200000, 1.0, 0,
                                  null, null, null, 0, null, null) == 1
     assert lib.kv_append_paged(good, null, null, -3, null, null, 1, null, 1,
                                null, null, 1, null, null) == 1
     assert lib.attn_merge_lse(2, 3, 4, 130, null, null, null, null, null) == 2
     assert lib.attn_merge_lse(-1, 3, 4, 128, null, null, null, null, null) == 1
     # empty work is a no-op success
-    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 0, 16, 1.0,
+    assert lib.attn_decode_paged(good, null, null, null, 1, null, 1, null, 0, 16, 1.0, 0,
                                  null, null, null, 0, null, null) == 0
     assert lib.attn_merge_lse(1, 0, 16, 128, null, null, null, null, null) == 0
     assert lib.pa_read_device_status(null, null, null) == 1
@@ -129,9 +129,9 @@ def test_decode_and_append_argument_errors_are_rejected_before_launch(lib):
     INVALID, OK = 1, 0
 
     def decode(q=a, k=a, v=a, num_pages=64, bt=a, bt_stride=8, sl=a, batch=1, max_s=1024,
-               scale=0.0884, out=a, work=ws):
+               scale=0.0884, split=0, out=a, work=ws):
         return lib.attn_decode_paged(good, q, k, v, num_pages, bt, bt_stride, sl, batch, max_s,
-                                     scale, out, null, work, 1 << 30, null, null)
+                                     scale, split, out, null, work, 1 << 30, null, null)
 
     assert decode(batch=-1) == INVALID
     assert decode(batch=4097) == INVALID                    # past the largest decode batch
@@ -140,6 +140,7 @@ def test_decode_and_append_argument_errors_are_rejected_before_launch(lib):
     assert decode(max_s=-1) == INVALID
     assert decode(max_s=131073) == INVALID
     assert decode(scale=float("nan")) == INVALID
+    assert decode(split=-1) == INVALID                      # split size must be >= 0 (0 = auto)
     for kw in ("q", "k", "v", "bt", "sl", "out", "work"):
         assert decode(**{kw: null}) == INVALID, kw
     for kw in ("q", "k", "v", "out"):

@@ -48,6 +48,25 @@ def test_kv_append_missing_table_entry_is_flagged(cuda_lib):
     assert np.array_equal(after[mask], before[mask])                  # nothing else touched
 
 
+def test_kv_append_more_packed_rows_than_total_new_is_flagged(cuda_lib):
+    """cu_new_lens[batch] = 50 but the call is given total_new = 40 rows: the first 40 rows are
+    placed exactly as the oracle places them, the other 10 are not written (no pool byte
+    outside the first 40 rows' slots changes) and PA_DEV_ERR_LENGTH is set."""
+    inp = W.make_paged(311, [100, 50], [30, 20], device="cuda")
+    k0, v0 = bits(inp.k_pools[0]).copy(), bits(inp.v_pools[0]).copy()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.kv_append_paged(inp.k_new[0][:40].contiguous(), inp.v_new[0][:40].contiguous(),
+                             inp.cu_q_lens, inp.start_pos, inp.block_table, inp.k_pools[0],
+                             inp.v_pools[0], status=status)
+    assert cuda_lib.read_device_status(status) & cuda_lib.DEV_ERR_LENGTH
+    # the oracle's placement of the rows that were given: sequence 1 keeps its first 10 rows
+    ek, ev = oracle.kv_append(bits(inp.k_new[0])[:40], bits(inp.v_new[0])[:40],
+                              np.array([0, 30, 40]), host(inp.start_pos), inp.host_block_table,
+                              k0, v0)
+    assert np.array_equal(bits(inp.k_pools[0]), ek)
+    assert np.array_equal(bits(inp.v_pools[0]), ev)
+
+
 @pytest.mark.parametrize("S,R,H", [(1, 5, 16), (3, 7, 16), (40, 2, 3), (2, 1, 1)])
 def test_merge_lse(cuda_lib, S, R, H):
     g = torch.Generator(device="cuda").manual_seed(S * 100 + R)

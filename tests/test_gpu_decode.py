@@ -1,5 +1,6 @@
 """Decode parity: the CUDA split-KV decode against the fp64 oracle, on the same seeded bytes."""
 import math
+import time
 
 import numpy as np
 import pytest
@@ -174,3 +175,74 @@ def test_decode_workspace_too_small_is_rejected(cuda_lib):
     with pytest.raises(cuda_lib.PagedAttnError):
         cuda_lib.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0], inp.block_table,
                                    inp.seq_lens, 100, inp.scale, workspace=ws)
+
+
+SPLITS = [0, 16, 256, 1024, 4096, 2**31 - 1]
+
+
+@pytest.mark.parametrize("lens", [[4000, 123, 2049, 0, 16, 30000, 1], [1000] * 4 + [70000]])
+def test_decode_split_count_invariance(cuda_lib, lens):
+    """split_tokens in {auto, 16, 256, 1024, 4096, one range}: the key ranges and so the number
+    of partials per sequence differ (from one page per range to a single CTA for the whole
+    batch); every result matches the oracle, and all agree with each other within the same
+    tolerance (the split sizes are whole pages)."""
+    pa = cuda_lib
+    inp = W.make_paged(17 + len(lens), lens, [1] * len(lens), poison=True, device="cuda")
+    ref_o, ref_l = oracle_decode(inp)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    results = {}
+    for split in SPLITS:
+        out, lse = pa.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0],
+                                        inp.block_table, inp.seq_lens, max(lens), inp.scale,
+                                        split_tokens=split, status=status)
+        torch.cuda.synchronize()
+        check_attn(out, lse, ref_o, ref_l, what=f"split_tokens={split}")
+        assert pa.read_device_status(status) == 0, split
+        results[split] = (out.clone(), lse.clone())
+    base_o = results[0][0].double().cpu().numpy()
+    base_l = results[0][1].double().cpu().numpy()
+    for split in SPLITS[1:]:
+        check_attn(results[split][0], results[split][1], base_o, base_l,
+                   what=f"split_tokens={split} vs auto")
+
+
+def test_decode_split_workspace_grows_with_the_range_count(cuda_lib):
+    """A smaller split needs records for more ranges; a workspace sized for auto is rejected
+    when the split needs more."""
+    pa = cuda_lib
+    auto = pa.decode_workspace_size(4, 30000)
+    fine = pa.decode_workspace_size(4, 30000, split_tokens=16)
+    assert fine > auto
+    assert pa.decode_workspace_size(4, 30000, split_tokens=2**31 - 1) < auto
+    inp = W.make_paged(16, [30000, 5, 700, 12000], [1] * 4, device="cuda")
+    ws = torch.empty(auto, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttnError):
+        pa.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0], inp.block_table,
+                             inp.seq_lens, 30000, inp.scale, split_tokens=16, workspace=ws)
+
+
+def test_decode_bounded_wait_gives_up_and_the_next_call_is_correct(cuda_lib):
+    """The test hook leaves one ring stage of CTA 0 unfilled and bounds the waits by 1 ms: the
+    waiting consumer warps give up, flag PA_DEV_ERR_TIMEOUT and return (the producer drains its
+    own copies first). The context stays usable: the next normal call on the same stream
+    matches the oracle."""
+    pa = cuda_lib
+    inp = W.make_paged(15, [3000, 40, 700], [1, 1, 1], device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.debug_decode_starve(True)
+    try:
+        t0 = time.perf_counter()
+        pa.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0], inp.block_table,
+                             inp.seq_lens, 3000, inp.scale, status=status)
+        flags = pa.read_device_status(status)
+        dt = time.perf_counter() - t0
+    finally:
+        pa.debug_decode_starve(False)
+    assert flags & pa.DEV_ERR_TIMEOUT, flags
+    assert dt < 1.5, dt
+    out, lse = pa.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0], inp.block_table,
+                                    inp.seq_lens, 3000, inp.scale, status=status)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(status) == 0
+    ref_o, ref_l = oracle_decode(inp)
+    check_attn(out, lse, ref_o, ref_l, what="after the timed-out call")

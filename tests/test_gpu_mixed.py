@@ -51,29 +51,46 @@ def test_mixed_step_reduced(cuda_lib):
         check_attn(do, dl, ro[2], ro[3], what=f"layer {layer} decode")
 
 
-def test_mixed_step_full_size_sampled(cuda_lib):
+def chunk_rows_256(n, rng):
+    """256 rows of a chunk of n: the first and last 16, the rows around every 16-key page edge
+    and 128-query tile edge that fall on them, the rest random."""
+    rows = set(range(16)) | set(range(n - 16, n))
+    edges = set()
+    for e in range(128, n, 128):
+        edges |= {e - 1, e, e + 1}
+    for e in range(16, n, 16 * 37):          # page edges spread across the chunk
+        edges |= {e - 1, e}
+    rows |= set(sorted(edges)[:96])
+    while len(rows) < 256:
+        rows.add(int(rng.integers(0, n)))
+    return sorted(rows)
+
+
+def test_mixed_step_full_size(cuda_lib):
     """The 28-layer mixed workload at full size (about 173 GB of pools), in the bench's launch
-    configuration; checked on sampled layers, sampled prefill rows and sampled sequences."""
+    configuration: on layers 0 and 27 and two more drawn by seed, every decode sequence and
+    256 rows of the chunk (every head) are checked against the oracle, which appends the new
+    tokens itself into the pools as they were before the step."""
     free, _ = torch.cuda.mem_get_info()
     L, ql = W.lengths_for("mixed_28l")
     need = 28 * 2 * int((-(-L // 16)).sum() + 16) * 32768 + (8 << 30)
     if free < need:
         pytest.skip(f"needs {need / 2**30:.0f} GiB free, have {free / 2**30:.0f} GiB")
     inp = W.make_workload("mixed_28l", device="cuda")
-    check_layers = {0, 13, 27}
+    rng = np.random.default_rng(5)
+    check_layers = {0, 27} | set(int(x) for x in rng.choice(np.arange(1, 27), size=2, replace=False))
     saved = {l: (bits(inp.k_pools[l]).copy(), bits(inp.v_pools[l]).copy()) for l in check_layers}
     outs = {}
     for layer in range(28):
         r = mixed_step(cuda_lib, inp, layer, 4096)
         if layer in check_layers:
-            outs[layer] = r
+            outs[layer] = tuple(t.clone() for t in r)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(5)
-    rows = sorted(set(range(8)) | set(range(4088, 4096)) | set(int(x) for x in rng.integers(0, 4096, 24)))
-    seqs = sorted(set(int(x) for x in rng.integers(0, 31, 6)) | {0, 30})
+    rows = chunk_rows_256(4096, rng)
+    assert len(rows) == 256
     for layer in sorted(check_layers):
         kb, vb = saved.pop(layer)
-        ro = oracle_mixed(inp, layer, kb, vb, 4096, prefill_rows=rows, decode_seqs=seqs)
+        ro = oracle_mixed(inp, layer, kb, vb, 4096, prefill_rows=rows)
         po, pl, do, dl = outs[layer]
         check_attn(po, pl, ro[0], ro[1], rows=rows, what=f"layer {layer} prefill")
-        check_attn(do, dl, ro[2], ro[3], rows=seqs, what=f"layer {layer} decode")
+        check_attn(do, dl, ro[2], ro[3], what=f"layer {layer} decode (all 31 sequences)")
