@@ -36,10 +36,12 @@
 namespace pa {
 namespace {
 
-constexpr int kConsumerWarps = kHkv;
+constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 3;
-constexpr uint32_t kPageBytes = kPage * kHkv * kHeadDim * 2;  // K (or V) of one page
+// A ring stage holds K (or V) of 16 tokens x 8 KV heads: one page of the decoder's pools, or
+// 8 / Hkv consecutive pages of a call with Hkv < 8 KV heads.
+constexpr uint32_t kStageBytes = kPage * kHkv * kHeadDim * 2;
 constexpr int kMaxBatch = 4096;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 #ifndef PA_DECODE_MIN_PAGES
@@ -48,7 +50,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMinPagesPerCta = PA_DECODE_MIN_PAGES;
 
 struct DecodeSmem {
-  uint8_t kv[kStages][2][kPageBytes];
+  uint8_t kv[kStages][2][kStageBytes];
   float p[kConsumerWarps][32];
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -58,6 +60,8 @@ struct DecodeSmem {
 };
 
 struct DecodeParams {
+  int32_t hq;           // query heads of the call (2 x its KV heads)
+  int32_t stage_pages;  // pages per ring stage: 8 / KV heads
   const uint16_t* q;
   const uint8_t* k_pool;
   const uint8_t* v_pool;
@@ -74,7 +78,7 @@ struct DecodeParams {
   float* lse;
   int32_t* ws_header;  // [0] = pages per range (W), [1] = total pages, [2] = grid size
   int32_t* ws_prefix;  // [batch + 1]
-  float* ws_lse;       // [records][Hq]
+  float* ws_lse;       // [records][Hq], record (b + range) * stage_pages + page slot
   float* ws_o;         // [records][Hq][D]
   int32_t* status;
   uint64_t wait_limit_ns;  // bound of every mbarrier wait
@@ -138,7 +142,14 @@ __device__ __forceinline__ int find_seq(const int32_t* prefix, int batch, int x)
   return lo;
 }
 
+// kHkvT: KV heads of the call (8 for the decoder; 1, 2 or 4 for a device's share of them).
+// Consumer warp w serves KV head w % kHkvT of page slot w / kHkvT of each stage.
+template <int kHkvT>
 __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const DecodeParams p) {
+  constexpr int kSlots = kHkv / kHkvT;                        // pages per stage
+  constexpr int kHqT = kGroup * kHkvT;
+  constexpr uint32_t kPageBytes = kPage * kHkvT * kHeadDim * 2;  // K (or V) of one page
+  constexpr int kTokenBytes = kHkvT * kHeadDim * 2;             // one token's row in a page
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   DecodeSmem& s = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -198,8 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
               entry = 0;
             }
           }
-          for (int i = 0; i < n; ++i) {
-            const int page = __shfl_sync(0xffffffffu, entry, i);
+          // one stage = kSlots consecutive pages of this sequence (32 is a multiple of kSlots,
+          // so the stages line up with the consumers' page groups)
+          for (int i = 0; i < n; i += kSlots) {
+            const int n_st = min(kSlots, n - i);
+            int page[kSlots];
+#pragma unroll
+            for (int j = 0; j < kSlots; ++j) page[j] = __shfl_sync(0xffffffffu, entry, min(i + j, 31));
             if (lane == 0) {
               if (starve) {
                 starve = false;  // this stage stays empty: its consumers' waits run out
@@ -207,11 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
                 flag_error(p.status, PA_DEV_ERR_TIMEOUT);
                 ok = false;
               } else {
-                mbar_arrive_expect_tx(&s.full[stage], 2 * kPageBytes);
-                bulk_g2s(s.kv[stage][0], p.k_pool + static_cast<int64_t>(page) * kPageBytes,
-                         kPageBytes, &s.full[stage]);
-                bulk_g2s(s.kv[stage][1], p.v_pool + static_cast<int64_t>(page) * kPageBytes,
-                         kPageBytes, &s.full[stage]);
+                mbar_arrive_expect_tx(&s.full[stage], 2 * n_st * kPageBytes);
+#pragma unroll
+                for (int j = 0; j < kSlots; ++j) {
+                  if (j < n_st) {
+                    bulk_g2s(s.kv[stage][0] + j * kPageBytes,
+                             p.k_pool + static_cast<int64_t>(page[j]) * kPageBytes, kPageBytes,
+                             &s.full[stage]);
+                    bulk_g2s(s.kv[stage][1] + j * kPageBytes,
+                             p.v_pool + static_cast<int64_t>(page[j]) * kPageBytes, kPageBytes,
+                             &s.full[stage]);
+                  }
+                }
                 ++issued;
               }
             }
@@ -237,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
   }
 
   // ------------------------------------------------------------------ consumer warps
-  const int g = warp;          // KV head
+  const int g = warp % kHkvT;  // KV head
+  const int slot = warp / kHkvT;  // page of each stage
   const int c = lane & 15;     // dims 8c .. 8c+7
   const int th = lane >> 4;    // tokens th*8 .. th*8+7 of each page
   const bool hi_head = (c & 8) != 0;  // head of the score this lane owns after the scatter
@@ -256,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
 
       float2 qa[4], qb[4];
       {
-        const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHq + 2 * g) * kHeadDim + 8 * c;
+        const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHqT + 2 * g) * kHeadDim + 8 * c;
         const uint4 ra = *reinterpret_cast<const uint4*>(qrow);
         const uint4 rb = *reinterpret_cast<const uint4*>(qrow + kHeadDim);
         const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
@@ -273,8 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
       float l_part = 0.f;                               // this lane's share of its head's sum
 
       bool all_ok = true;
-      for (int lp = lp0; lp < lp1; ++lp) {
-        const int n_valid = min(kPage, L - lp * kPage);
+      for (int lp0s = lp0; lp0s < lp1; lp0s += kSlots) {
+        const int lp = lp0s + slot;               // this warp's page of the stage
+        const bool active = lp < lp1;             // (a stage may hold fewer than kSlots pages)
+        const int n_valid = active ? min(kPage, L - lp * kPage) : 0;
         bool ok = true;
         if (!mbar_wait_bounded(&s.full[stage], phase, p.wait_limit_ns)) {
           flag_error(p.status, PA_DEV_ERR_TIMEOUT);
@@ -284,90 +310,91 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
           all_ok = false;
           break;
         }
-        const uint8_t* Ks = s.kv[stage][0] + g * (kHeadDim * 2) + c * 16;
-        const uint8_t* Vs = s.kv[stage][1] + g * (kHeadDim * 2) + c * 16;
-
-        // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
-        float v[16];
+        const uint8_t* Ks = s.kv[stage][0] + slot * kPageBytes + g * (kHeadDim * 2) + c * 16;
+        const uint8_t* Vs = s.kv[stage][1] + slot * kPageBytes + g * (kHeadDim * 2) + c * 16;
+        if (active) {
+          // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
+          float v[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 kr = lds128(Ks + (th * 8 + j) * (kHkv * kHeadDim * 2));
-          const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
-          const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
-          const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
-          const float2 k3 = make_float2(bf16lo(kr.w), bf16hi(kr.w));
-          float2 sa = mul2(qa[0], k0), sb = mul2(qb[0], k0);
-          sa = fma2(qa[1], k1, sa); sb = fma2(qb[1], k1, sb);
-          sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
-          sa = fma2(qa[3], k3, sa); sb = fma2(qb[3], k3, sb);
-          v[j] = sa.x + sa.y;
-          v[8 + j] = sb.x + sb.y;
-        }
-        // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score
-        //      of token th*8 + (c & 7), head (c >> 3).
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1) {
-          const bool up = (c & w) != 0;
-#pragma unroll
-          for (int i = 0; i < w; ++i) {
-            const float send = up ? v[i] : v[w + i];
-            const float keep = up ? v[w + i] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+          for (int j = 0; j < 8; ++j) {
+            const uint4 kr = lds128(Ks + (th * 8 + j) * kTokenBytes);
+            const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
+            const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
+            const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
+            const float2 k3 = make_float2(bf16lo(kr.w), bf16hi(kr.w));
+            float2 sa = mul2(qa[0], k0), sb = mul2(qb[0], k0);
+            sa = fma2(qa[1], k1, sa); sb = fma2(qb[1], k1, sb);
+            sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
+            sa = fma2(qa[3], k3, sa); sb = fma2(qb[3], k3, sb);
+            v[j] = sa.x + sa.y;
+            v[8 + j] = sb.x + sb.y;
           }
-        }
-        float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
-
-        // ---- page max per head, lazily moved running max
-        float pm = sc;
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-        const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
-        const float pmax_a = hi_head ? pm_other : pm;
-        const float pmax_b = hi_head ? pm : pm_other;
-        if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
-          const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
-          const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
-          const float al_b = (m_b == -CUDART_INF_F) ? 0.f : fast_exp2(m_b - nb);
-          const float2 fa = make_float2(al_a, al_a), fb = make_float2(al_b, al_b);
+          // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score
+          //      of token th*8 + (c & 7), head (c >> 3).
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc_a[i] = mul2(acc_a[i], fa);
-            acc_b[i] = mul2(acc_b[i], fb);
+          for (int w = 8; w >= 1; w >>= 1) {
+            const bool up = (c & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = up ? v[i] : v[w + i];
+              const float keep = up ? v[w + i] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
           }
-          l_part *= hi_head ? al_b : al_a;
-          m_a = na;
-          m_b = nb;
-        }
-        const float pr = fast_exp2(sc - (hi_head ? m_b : m_a));
-        l_part += pr;
+          float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
 
-        // ---- hand probabilities to the lanes that own the V dims
-        s.p[warp][lane] = pr;
-        __syncwarp();
-        const float4 pa0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 0]);
-        const float4 pa1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 4]);
-        const float4 pb0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 8]);
-        const float4 pb1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 12]);
-        const float pav[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
-        const float pbv[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
-
-        // ---- o += p v over this lane's 8 tokens (invalid slots of a partial page skipped)
+          // ---- page max per head, lazily moved running max
+          float pm = sc;
+          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+          const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
+          const float pmax_a = hi_head ? pm_other : pm;
+          const float pmax_b = hi_head ? pm : pm_other;
+          if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
+            const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
+            const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
+            const float al_b = (m_b == -CUDART_INF_F) ? 0.f : fast_exp2(m_b - nb);
+            const float2 fa = make_float2(al_a, al_a), fb = make_float2(al_b, al_b);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (th * 8 + j < n_valid) {
-            const uint4 vr = lds128(Vs + (th * 8 + j) * (kHkv * kHeadDim * 2));
-            const float2 ppa = make_float2(pav[j], pav[j]);
-            const float2 ppb = make_float2(pbv[j], pbv[j]);
-            const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
-            const float2 v1 = make_float2(bf16lo(vr.y), bf16hi(vr.y));
-            const float2 v2 = make_float2(bf16lo(vr.z), bf16hi(vr.z));
-            const float2 v3 = make_float2(bf16lo(vr.w), bf16hi(vr.w));
-            acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
-            acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
-            acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
-            acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
+            for (int i = 0; i < 4; ++i) {
+              acc_a[i] = mul2(acc_a[i], fa);
+              acc_b[i] = mul2(acc_b[i], fb);
+            }
+            l_part *= hi_head ? al_b : al_a;
+            m_a = na;
+            m_b = nb;
+          }
+          const float pr = fast_exp2(sc - (hi_head ? m_b : m_a));
+          l_part += pr;
+
+          // ---- hand probabilities to the lanes that own the V dims
+          s.p[warp][lane] = pr;
+          __syncwarp();
+          const float4 pa0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 0]);
+          const float4 pa1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 4]);
+          const float4 pb0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 8]);
+          const float4 pb1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 12]);
+          const float pav[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
+          const float pbv[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
+
+          // ---- o += p v over this lane's 8 tokens (invalid slots of a partial page skipped)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (th * 8 + j < n_valid) {
+              const uint4 vr = lds128(Vs + (th * 8 + j) * kTokenBytes);
+              const float2 ppa = make_float2(pav[j], pav[j]);
+              const float2 ppb = make_float2(pbv[j], pbv[j]);
+              const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
+              const float2 v1 = make_float2(bf16lo(vr.y), bf16hi(vr.y));
+              const float2 v2 = make_float2(bf16lo(vr.z), bf16hi(vr.z));
+              const float2 v3 = make_float2(bf16lo(vr.w), bf16hi(vr.w));
+              acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
+              acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
+              acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
+              acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
+            }
           }
         }
         __syncwarp();
@@ -396,7 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
       const int head = 2 * g + th;
       const float l_h = th ? l_b : l_a;
       const float m_h = th ? m_b : m_a;
-      const float inv = 1.0f / l_h;
+      // (with several pages per stage a warp may have seen no page of this range: l = 0, and
+      // its record is o = 0, lse = -inf, which the merge weighs by 0)
+      const float inv = (kSlots == 1 || l_h > 0.f) ? 1.0f / l_h : 0.f;
       float o[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -405,20 +434,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
         o[2 * i + 1] = a.y * inv;
       }
       const float lse_h = (m_h + log2f(l_h)) * kLn2;
-      if (lp0 == 0 && lp1 == n_pages) {
+      if (kSlots == 1 && lp0 == 0 && lp1 == n_pages) {
         uint4 w;
         w.x = pack_bf16x2(o[0], o[1]);
         w.y = pack_bf16x2(o[2], o[3]);
         w.z = pack_bf16x2(o[4], o[5]);
         w.w = pack_bf16x2(o[6], o[7]);
-        *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + head) * kHeadDim + 8 * c) = w;
-        if (c == 0 && p.lse != nullptr) p.lse[b * kHq + head] = lse_h;
+        *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHqT + head) * kHeadDim + 8 * c) = w;
+        if (c == 0 && p.lse != nullptr) p.lse[b * kHqT + head] = lse_h;
       } else {
-        const int64_t r = static_cast<int64_t>(b) + rg;  // unique per (sequence, range)
-        float* dst = p.ws_o + (r * kHq + head) * kHeadDim + 8 * c;
+        // unique per (sequence, range, page slot): the records of sequence b are
+        // b * kSlots + k for k = range * kSlots + slot over the ranges that touch it
+        const int64_t r = (static_cast<int64_t>(b) + rg) * kSlots + slot;
+        float* dst = p.ws_o + (r * kHqT + head) * kHeadDim + 8 * c;
         reinterpret_cast<float4*>(dst)[0] = make_float4(o[0], o[1], o[2], o[3]);
         reinterpret_cast<float4*>(dst)[1] = make_float4(o[4], o[5], o[6], o[7]);
-        if (c == 0) p.ws_lse[r * kHq + head] = lse_h;
+        if (c == 0) p.ws_lse[r * kHqT + head] = lse_h;
       }
     }
   }
@@ -442,22 +473,25 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
   __shared__ float4 red_o[kWarps][32];
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq = p.hq, slots = p.stage_pages;
   const int p0 = p.ws_prefix[b], p1 = p.ws_prefix[b + 1];
-  uint16_t* orow = p.out + (static_cast<int64_t>(b) * kHq + h) * kHeadDim + 4 * lane;
+  uint16_t* orow = p.out + (static_cast<int64_t>(b) * hq + h) * kHeadDim + 4 * lane;
   if (p1 == p0) {
     if (warp == 0) {
       *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
-      if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = -CUDART_INF_F;
+      if (lane == 0 && p.lse != nullptr) p.lse[b * hq + h] = -CUDART_INF_F;
     }
     return;
   }
   const int W = p.ws_header[0];
-  const int c0 = p0 / W, c1 = (p1 - 1) / W;
-  if (c0 == c1) return;  // finished inside one CTA
+  const int r0 = p0 / W, r1 = (p1 - 1) / W;
+  if (r0 == r1 && slots == 1) return;  // finished inside one CTA
+  // partials c0 .. c1: record b * slots + c, c = range * slots + page slot
+  const int c0 = r0 * slots, c1 = r1 * slots + slots - 1;
   // this warp's partials c0 + warp, c0 + warp + kWarps, ..., four at a time: sum of
   // 2^(lse_c - m) o_c (lse in log2 units) against a running maximum m, rescaled when m moves
-  const float* lse_src = p.ws_lse + static_cast<int64_t>(b) * kHq + h;
-  const float* o_src = p.ws_o + (static_cast<int64_t>(b) * kHq + h) * kHeadDim + 4 * lane;
+  const float* lse_src = p.ws_lse + static_cast<int64_t>(b) * slots * hq + h;
+  const float* o_src = p.ws_o + (static_cast<int64_t>(b) * slots * hq + h) * kHeadDim + 4 * lane;
   float m = -CUDART_INF_F, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c = c0 + warp; c <= c1; c += 4 * kWarps) {
@@ -466,8 +500,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int cu = c + u * kWarps;
-      l2[u] = cu <= c1 ? lse_src[static_cast<int64_t>(cu) * kHq] * kLog2e : -CUDART_INF_F;
-      o[u] = cu <= c1 ? *reinterpret_cast<const float4*>(o_src + static_cast<int64_t>(cu) * kHq * kHeadDim)
+      l2[u] = cu <= c1 ? lse_src[static_cast<int64_t>(cu) * hq] * kLog2e : -CUDART_INF_F;
+      o[u] = cu <= c1 ? *reinterpret_cast<const float4*>(o_src + static_cast<int64_t>(cu) * hq * kHeadDim)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     const float mn = fmaxf(fmaxf(m, fmaxf(l2[0], l2[1])), fmaxf(l2[2], l2[3]));
@@ -506,7 +540,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
   const float inv = 1.0f / wsum;
   *reinterpret_cast<uint2*>(orow) =
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  if (lane == 0 && p.lse != nullptr) p.lse[b * kHq + h] = (M + log2f(wsum)) * kLn2;
+  if (lane == 0 && p.lse != nullptr) p.lse[b * hq + h] = (M + log2f(wsum)) * kLn2;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -515,20 +549,19 @@ struct WsLayout {
   size_t header, prefix, lse, o, total;
 };
 
-WsLayout ws_layout(int batch, int64_t ranges) {
+// Records: (batch + ranges) x pages per stage, each [Hq] lse and [Hq][128] o. For a call with
+// Hkv < 8 KV heads there are 8 / Hkv page slots per range but only 2 Hkv query heads, so the
+// workspace is never larger than the decoder's.
+WsLayout ws_layout(int batch, int64_t ranges, int hkv) {
   WsLayout w;
-  const size_t records = static_cast<size_t>(batch) + static_cast<size_t>(ranges);
+  const int hq = kGroup * hkv, slots = kHkv / hkv;
+  const size_t records = (static_cast<size_t>(batch) + static_cast<size_t>(ranges)) * slots;
   w.header = 0;
   w.prefix = 256;
   w.lse = align_up(w.prefix + sizeof(int32_t) * (batch + 1), 256);
-  w.o = align_up(w.lse + sizeof(float) * records * kHq, 256);
-  w.total = align_up(w.o + sizeof(float) * records * kHq * kHeadDim, 256);
+  w.o = align_up(w.lse + sizeof(float) * records * hq, 256);
+  w.total = align_up(w.o + sizeof(float) * records * hq * kHeadDim, 256);
   return w;
-}
-
-bool dims_supported(const pa_dims& d) {
-  return d.num_q_heads == kHq && d.num_kv_heads == kHkv && d.head_dim == kHeadDim &&
-         d.page_size == kPage;
 }
 
 // With an explicit split size, at most this many ranges per SM (the split is raised beyond
@@ -579,11 +612,11 @@ int decode_grid_size() { return sm_count_current_device(); }
 
 extern "C" size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len,
                                            int32_t split_tokens) {
-  (void)dims;
-  if (batch < 0 || max_seq_len < 0 || split_tokens < 0) return 0;
+  if (!pa::gqa_dims_supported(dims) || batch < 0 || max_seq_len < 0 || split_tokens < 0) return 0;
   const int sm_grid = pa::decode_grid_size();
   if (sm_grid <= 0) return 0;
-  return pa::ws_layout(batch, pa::decode_plan(batch, max_seq_len, split_tokens, sm_grid).ws_ranges).total;
+  return pa::ws_layout(batch, pa::decode_plan(batch, max_seq_len, split_tokens, sm_grid).ws_ranges,
+                       dims.num_kv_heads).total;
 }
 
 extern "C" pa_status pa_debug_decode_starve(int32_t enable) {
@@ -600,7 +633,7 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
                                        void* workspace, size_t workspace_bytes, int32_t* status,
                                        pa_stream_t stream) {
   using namespace pa;
-  if (!dims_supported(dims)) return PA_ERR_UNSUPPORTED;
+  if (!gqa_dims_supported(dims)) return PA_ERR_UNSUPPORTED;
   if (batch < 0 || batch > kMaxBatch || bt_stride <= 0 || num_pages <= 0 || max_seq_len < 0 ||
       max_seq_len > 131072 || !(softmax_scale == softmax_scale) || split_tokens < 0)
     return PA_ERR_INVALID_ARG;
@@ -614,16 +647,23 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   const int sm_grid = decode_grid_size();
   if (sm_grid <= 0) return PA_ERR_CUDA;
   const DecodePlan plan = decode_plan(batch, max_seq_len, split_tokens, sm_grid);
-  if (workspace_bytes < ws_layout(batch, plan.ws_ranges).total) return PA_ERR_WORKSPACE_TOO_SMALL;
-  const WsLayout w = ws_layout(batch, plan.max_ranges);
+  const int hkv = dims.num_kv_heads;
+  if (workspace_bytes < ws_layout(batch, plan.ws_ranges, hkv).total) return PA_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout w = ws_layout(batch, plan.max_ranges, hkv);
 
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(DecodeSmem)));
+    const int smem = static_cast<int>(sizeof(DecodeSmem));
+    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_splitkv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_splitkv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_splitkv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(decode)");
     // the merge kernel uses no shared memory; giving it the split kernel's carveout keeps the
     // SMs from reconfiguring shared memory / L1 between the two launches of every call
@@ -639,6 +679,8 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   }
 
   DecodeParams p;
+  p.hq = dims.num_q_heads;
+  p.stage_pages = kHkv / hkv;
   p.q = static_cast<const uint16_t*>(q);
   p.k_pool = static_cast<const uint8_t*>(k_pool);
   p.v_pool = static_cast<const uint8_t*>(v_pool);
@@ -663,14 +705,21 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   p.starve = g_debug_starve ? 1 : 0;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  decode_splitkv_kernel<<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p);
+  switch (hkv) {
+    case 8: decode_splitkv_kernel<8><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
+    case 4: decode_splitkv_kernel<4><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
+    case 2: decode_splitkv_kernel<2><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
+    default: decode_splitkv_kernel<1><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
+  }
   PA_CHECK_LAUNCH("decode_splitkv_kernel");
   {
     cudaLaunchConfig_t cfg = {};
     // partials per sequence when the lengths are equal: ceil(ranges / batch), plus one for a
-    // cut at each end; more than 4 warps take in one round of 4 loads -> 16 warps per head
-    const bool small = (plan.max_ranges + batch - 1) / batch + 1 > 4 * kMergeWarpsLarge;
-    cfg.gridDim = dim3(batch, kHq);
+    // cut at each end, times the page slots per range; more than 4 warps take in one round of
+    // 4 loads -> 16 warps per head
+    const bool small =
+        ((plan.max_ranges + batch - 1) / batch + 1) * p.stage_pages > 4 * kMergeWarpsLarge;
+    cfg.gridDim = dim3(batch, dims.num_q_heads);
     cfg.blockDim = dim3((small ? kMergeWarpsSmall : kMergeWarpsLarge) * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -739,7 +788,7 @@ extern "C" pa_status attn_decode_paged_noalloc(pa_dims dims, const void* q, cons
   if (batch > 0) {
     const int grid = decode_grid_size();
     if (grid <= 0) return PA_ERR_CUDA;
-    const size_t need = ws_layout(batch, decode_plan(batch, max_seq_len, 0, grid).ws_ranges).total;
+    const size_t need = pa_decode_workspace_size(dims, batch, max_seq_len, 0);
     if (need > kStaticScratchBytes) {
       snprintf_error("attn_decode_paged_noalloc: batch %d needs %zu bytes of scratch on this GPU, "
                      "more than the built-in %zu bytes; use attn_decode_paged with a workspace",

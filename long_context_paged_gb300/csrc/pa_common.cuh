@@ -11,9 +11,18 @@ namespace pa {
 
 constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
-constexpr int kHkv = 8;
+constexpr int kHkv = 8;             // KV heads of the decoder (at most this many per call)
 constexpr int kHq = 16;
 constexpr int kGroup = kHq / kHkv;  // query heads per KV head
+
+// Head counts a call accepts: the decoder's GQA 16/8, or the slice of it that one device holds
+// when the KV heads are partitioned across devices (8/N KV heads with their 16/N query heads,
+// N = 1, 2, 4, 8); head_dim 128 and 16-token pages.
+inline bool gqa_dims_supported(const pa_dims& d) {
+  const int h = d.num_kv_heads;
+  return (h == 1 || h == 2 || h == 4 || h == 8) && d.num_q_heads == kGroup * h &&
+         d.head_dim == kHeadDim && d.page_size == kPage;
+}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

@@ -10,7 +10,7 @@
 #include "pa_common.cuh"
 
 namespace pa {
-pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_lens,
+pa_status launch_prefill_tc(int32_t hkv, const void* q, int32_t total_q, const int32_t* cu_q_lens,
                             const void* k_pool, const void* v_pool, int64_t num_pages,
                             const int32_t* block_table, int32_t bt_stride,
                             const int32_t* seq_lens, int32_t batch, int32_t max_q_len,
@@ -34,9 +34,7 @@ extern "C" pa_status attn_prefill_chunk(pa_dims dims, const void* q, const int32
                                         void* workspace, size_t workspace_bytes,
                                         int32_t* status, pa_stream_t stream) {
   using namespace pa;
-  if (dims.num_q_heads != kHq || dims.num_kv_heads != kHkv || dims.head_dim != kHeadDim ||
-      dims.page_size != kPage)
-    return PA_ERR_UNSUPPORTED;
+  if (!gqa_dims_supported(dims)) return PA_ERR_UNSUPPORTED;
   if (total_q < 0 || batch < 0 || bt_stride <= 0 || num_pages <= 0 || max_q_len < 0 ||
       max_seq_len < 0 || max_seq_len > 131072 || max_q_len > max_seq_len ||
       !(softmax_scale > 0.f) || !(softmax_scale < 1e30f))
@@ -47,7 +45,7 @@ extern "C" pa_status attn_prefill_chunk(pa_dims dims, const void* q, const int32
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pool) |
        reinterpret_cast<uintptr_t>(v_pool) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return PA_ERR_INVALID_ARG;
-  return launch_prefill_tc(q, total_q, cu_q_lens, k_pool, v_pool, num_pages, block_table,
+  return launch_prefill_tc(dims.num_kv_heads, q, total_q, cu_q_lens, k_pool, v_pool, num_pages, block_table,
                            bt_stride, seq_lens, batch, max_q_len, softmax_scale, out, lse,
                            workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -7,7 +7,8 @@
 // contractions here (thousands of queries per KV read), so they run on tcgen05.mma.
 //
 // Work decomposition. A job is 128 queries of one chunk x both query heads of one KV head
-// (GQA 16/8): two 128-row M tiles that share every K/V tile read. A job's causal key range is
+// (GQA 16/8, or 2N/N heads when the KV heads are partitioned across devices): two 128-row M
+// tiles that share every K/V tile read. A job's causal key range is
 // J tiles of 128 keys; one (job, key tile) pair is a unit. Jobs are ordered sequence, then KV
 // head, then query tile. A persistent grid of one CTA per SM first runs whole jobs round-robin
 // (CTA c takes jobs c, c + G, ...; all CTAs of a round start at key tile 0 together, so the CTAs
@@ -104,6 +105,7 @@ struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
 static_assert(sizeof(PrefillTcSmem) + 1024 <= 232448, "prefill shared memory over the 227 KB limit");
 
 struct PrefillTcParams {
+  int32_t hkv, hq;        // KV heads and query heads of the call (hq = 2 hkv)
   const int32_t* cu_q_lens;
   const int32_t* seq_lens;
   const int32_t* block_table;
@@ -264,7 +266,7 @@ struct JobWalker {
     SeqGeom s = cur.s;
     if (qt >= s.nqt) {
       qt = 0;
-      if (++g >= kHkv) {
+      if (++g >= p->hkv) {
         g = 0;
         do {
           ++b;
@@ -305,8 +307,8 @@ __device__ void build_unit_prefix(const PrefillTcParams& p, PrefillTcSmem& s) {
   int local_jobs = 0;
   for (int b = b0; b < b1; ++b) {
     const SeqGeom g = seq_geom(p, b, blockIdx.x == 0);
-    local += kHkv * g.T;
-    local_jobs += kHkv * g.nqt;
+    local += p.hkv * g.T;
+    local_jobs += p.hkv * g.nqt;
   }
   const long long incl = warp_incl_scan64((static_cast<long long>(local_jobs) << 40) | local, lane);
   // (jobs in the top 24 bits, units in the low 40: both sums fit: units < 2^40, jobs < 2^23)
@@ -329,8 +331,8 @@ __device__ void build_unit_prefix(const PrefillTcParams& p, PrefillTcSmem& s) {
     const SeqGeom g = seq_geom(p, b, false);
     s.unit_prefix[b] = run;
     s.job_prefix[b] = jrun;
-    run += kHkv * g.T;
-    jrun += kHkv * g.nqt;
+    run += p.hkv * g.T;
+    jrun += p.hkv * g.nqt;
   }
   __syncthreads();
   if (tid == 0) {
@@ -800,7 +802,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       const bool whole = pc.jb == 0 && pc.je == pc.J;
       const int head = 2 * pc.g + t;
       if (whole) {
-        uint16_t* dst = p.out + (static_cast<int64_t>(pc.s.q0 + qrow) * kHq + head) * kHeadDim;
+        uint16_t* dst = p.out + (static_cast<int64_t>(pc.s.q0 + qrow) * p.hq + head) * kHeadDim;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o32[32];
@@ -819,7 +821,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           }
         }
         if (live && p.lse != nullptr)
-          p.lse[static_cast<int64_t>(pc.s.q0 + qrow) * kHq + head] = (m_used + log2f(l)) * kLn2;
+          p.lse[static_cast<int64_t>(pc.s.q0 + qrow) * p.hq + head] = (m_used + log2f(l)) * kLn2;
       } else {
         // a piece of a job shared with neighbouring CTAs: slot 1 if it starts the job, else 0.
         // A row that saw no key in this piece contributes nothing: o = 0, lse = -inf.
@@ -917,7 +919,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
   }
   const float inv = 1.0f / sum;
   const int head = 2 * g + t;
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(s.q0 + qrow) * kHq + head) * kHeadDim);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(s.q0 + qrow) * p.hq + head) * kHeadDim);
 #pragma unroll
   for (int k = 0; k < kHeadDim / 8; ++k) {
     uint4 w;
@@ -927,7 +929,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
     w.w = pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
     dst[k] = w;
   }
-  if (p.lse != nullptr) p.lse[static_cast<int64_t>(s.q0 + qrow) * kHq + head] = m + logf(sum);
+  if (p.lse != nullptr) p.lse[static_cast<int64_t>(s.q0 + qrow) * p.hq + head] = m + logf(sum);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -961,7 +963,7 @@ size_t prefill_workspace_bytes(int batch) {
   return prefill_ws(batch, grid).total;
 }
 
-pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_lens,
+pa_status launch_prefill_tc(int32_t hkv, const void* q, int32_t total_q, const int32_t* cu_q_lens,
                             const void* k_pool, const void* v_pool, int64_t num_pages,
                             const int32_t* block_table, int32_t bt_stride,
                             const int32_t* seq_lens, int32_t batch, int32_t max_q_len,
@@ -978,9 +980,10 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   if (workspace == nullptr || workspace_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
   CUtensorMap qm, km, vm;
-  if (!make_map_3d(&qm, q, static_cast<uint64_t>(total_q), kHq, kTileM) ||
-      !make_map_3d(&km, k_pool, static_cast<uint64_t>(num_pages) * kPage, kHkv, kPage) ||
-      !make_map_3d(&vm, v_pool, static_cast<uint64_t>(num_pages) * kPage, kHkv, kPage)) {
+  const int hq = kGroup * hkv;
+  if (!make_map_3d(&qm, q, static_cast<uint64_t>(total_q), hq, kTileM) ||
+      !make_map_3d(&km, k_pool, static_cast<uint64_t>(num_pages) * kPage, hkv, kPage) ||
+      !make_map_3d(&vm, v_pool, static_cast<uint64_t>(num_pages) * kPage, hkv, kPage)) {
     snprintf_error("cuTensorMapEncodeTiled failed for the prefill operands");
     return PA_ERR_CUDA;
   }
@@ -1009,6 +1012,8 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
     configured_device = dev;
   }
   PrefillTcParams p;
+  p.hkv = hkv;
+  p.hq = hq;
   p.cu_q_lens = cu_q_lens;
   p.seq_lens = seq_lens;
   p.block_table = block_table;
@@ -1028,7 +1033,7 @@ pa_status launch_prefill_tc(const void* q, int32_t total_q, const int32_t* cu_q_
   prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(qm, km, vm, p);
   PA_CHECK_LAUNCH("prefill_tc_kernel");
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((max_q_len + kTileM - 1) / kTileM, kHkv, batch);
+  cfg.gridDim = dim3((max_q_len + kTileM - 1) / kTileM, hkv, batch);
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
