@@ -41,6 +41,8 @@ import workloads as W  # noqa: E402
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s HBM3e figure decode is quoted against
+BUCKETS = (1, 2, 4, 8, 16, 32)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -84,8 +86,11 @@ def source_hash(*names) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_from_profile(kernel_file: str, src_hash: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+def traffic_from_profile(kernel_file: str, src_hash: str, algorithmic_bytes: float):
+    """DRAM bytes per launch, scaled from a committed ncu summary of a small case of the same
+    kernel: the summary records DRAM bytes (read + write) per algorithmic byte of that case,
+    and traffic grows with the bytes the launch must move. None if the summary is missing or
+    was taken on another source."""
     path = os.path.join(ROOT, "profiles", kernel_file)
     if not os.path.exists(path):
         return None
@@ -97,7 +102,7 @@ def traffic_from_profile(kernel_file: str, src_hash: str):
     if vals.get("source_hash") != src_hash:
         return None
     try:
-        return float(vals["dram_bytes_per_launch_full_size"])
+        return round(float(vals["dram_bytes_per_algorithmic_byte"]) * algorithmic_bytes)
     except (KeyError, ValueError):
         return None
 
@@ -188,6 +193,9 @@ class Step:
         self.dec_bytes = decode_kv_bytes(L[self.dec_idx]) if len(self.dec_idx) else 0
         self.pairs = sum(prefill_pairs(int(L[i]), int(ql[i])) for i in self.chunk_idx)
         self.pf_flops = prefill_flops(self.pairs)
+        # bytes the prefill launch must move: the chunk's queries, its sequence's K/V, outputs
+        self.pf_bytes = sum(int(ql[i]) * W.HQ * W.HEAD_DIM * 2 * 2 + int(ql[i]) * W.HQ * 4
+                            + int(L[i]) * W.kv_bytes_per_token() for i in self.chunk_idx)
         B = inp.batch
         nd = len(self.dec_idx)
         if nd:
@@ -440,6 +448,8 @@ def main():
                                                      "prefill_ragged_mix"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-buckets", action="store_true",
+                    help="skip the decode batch-bucket latencies added to the default line")
     ap.add_argument("--clocks-out", default=None)
     args = ap.parse_args()
 
@@ -500,6 +510,10 @@ def main():
     if pa.read_device_status(step.status):
         raise RuntimeError("device status flagged errors in the timed region")
 
+    buckets = None
+    if args.workload == "mixed_28l" and not args.no_buckets:
+        buckets = bucket_latencies(pa, dev, dist, args.warmup)
+
     e2e = None
     if not args.no_e2e:
         e_dec, e_pf, h2d, d2h = e2e_run(step, max(1, min(args.steps, 3)))
@@ -526,9 +540,12 @@ def main():
         ach = step.dec_bytes / per_launch_s / 1e9
         roofs.append((t_dec, {"kernel": "attn_decode_paged (decode_splitkv + merge)", "bound": "hbm",
                               "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                              "frac": round(ach / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
-                              "traffic": traffic_from_profile("decode_splitkv_decode_b16_l27k.md", dec_src)
-                              if args.workload == "mixed_28l" else None,
+                              "frac": round(ach / hbm, 4), "peak_source": f"{peak_src} hbm_gbs (a read+write copy)",
+                              "frac_of_nominal_8tbs": round(ach / NOMINAL_HBM_GBS, 4),
+                              "traffic": traffic_from_profile("decode_splitkv_decode_b16_l27k.md", dec_src,
+                                                              step.dec_bytes),
+                              "traffic_source": "ncu dram bytes of decode_b16_l27k per algorithmic byte x "
+                                                "this launch's algorithmic bytes",
                               "algorithmic_bytes_per_launch": step.dec_bytes}))
     if t_pf:
         per_launch_s = t_pf / (step.layers * K_)
@@ -538,9 +555,12 @@ def main():
                              "achieved": round(ach, 2), "peak": pk, "unit": "TFLOP/s",
                              "frac": round(ach / pk, 4),
                              "peak_source": f"{peak_src} bf16_tflops" + ("_sustained" if step.layers > 1 else ""),
-                             "traffic": traffic_from_profile("prefill_tc_prefill_4096_at_61440.md", pf_src)
-                             if args.workload == "mixed_28l" else None,
-                             "algorithmic_flops_per_launch": step.pf_flops}))
+                             "traffic": traffic_from_profile("prefill_tc_prefill_4096_at_32768.md", pf_src,
+                                                             step.pf_bytes),
+                             "traffic_source": "ncu dram bytes of prefill_4096_at_32768 (the mixed step's "
+                                               "prefill launch alone) per algorithmic byte x this launch's",
+                             "algorithmic_flops_per_launch": step.pf_flops,
+                             "algorithmic_bytes_per_launch": step.pf_bytes}))
     roofs.sort(key=lambda x: -x[0])
 
     L = step.inp.host_seq_lens
@@ -567,11 +587,13 @@ def main():
                               "decode": round(t_dec * 1e3 / K_, 3) if t_dec else None,
                               "prefill": round(t_pf * 1e3 / K_, 3) if t_pf else None},
         "decode": None if dec_gbs is None else {"value": round(dec_gbs, 1), "unit": "GB/s",
-                                                 "frac_of_hbm_peak": round(dec_gbs / hbm, 4)},
+                                                 "frac_of_hbm_peak": round(dec_gbs / hbm, 4),
+                                                 "frac_of_nominal_8tbs": round(dec_gbs / NOMINAL_HBM_GBS, 4)},
         "prefill": None if pf_tflops is None else {"value": round(pf_tflops, 2), "unit": "TFLOP/s",
                                                     "frac_of_bf16_peak": round(pf_tflops / (bf16s if step.layers > 1 else bf16), 4)},
         "roofline": roofs[0][1] if roofs else None,
         "roofline_other": [r[1] for r in roofs[1:]],
+        "decode_buckets": buckets,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -670,54 +692,71 @@ def run_prefill_ragged(pa, args, dev, dist, world, rank):
             "gpu_launches": 2 * args.steps, "clocks": clocks}), flush=True)
 
 
+def bucket_latencies(pa, dev, dist, warmup, layers=28, seq_len=1000):
+    """Decode latency by batch bucket, the way a serving engine replays CUDA graphs: B = 1, 2,
+    4, 8, 16, 32 sequences of ``seq_len`` cached tokens (80 s of audio each), each layer with
+    its own pools. Two figures per bucket: microseconds per decode call inside one graph of
+    ``layers`` calls (one per layer, as in a decoder step's graph), and microseconds per replay
+    of a graph holding a single call (which adds the graph launch itself)."""
+    per_call, single, gbs = {}, {}, {}
+    for B in BUCKETS:
+        seed = W.CONFIG_SEED["decode_b1_l1000"] + B
+        inp = W.make_paged(seed, np.full(B, seq_len), np.ones(B, np.int64), layers=layers,
+                           device=dev, with_new_kv=False)
+        out = torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, W.HQ, dtype=torch.float32, device=dev)
+        ws = torch.empty(pa.decode_workspace_size(B, seq_len), dtype=torch.uint8, device=dev)
+        call = lambda l: pa.attn_decode_paged(inp.q[l], inp.k_pools[l], inp.v_pools[l],
+                                              inp.block_table, inp.seq_lens, seq_len, inp.scale,
+                                              out=out, lse=lse, workspace=ws)
+        call(0)
+        torch.cuda.synchronize()
+        g_all, g_one = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all):
+            for l in range(layers):
+                call(l)
+        with torch.cuda.graph(g_one):
+            call(0)
+        reps = 200
+        (t_all,) = max_over_ranks(dist, [timed_replays(g_all, reps, max(warmup, 3) * 5, dist)], dev)
+        (t_one,) = max_over_ranks(dist, [timed_replays(g_one, reps * 10, max(warmup, 3) * 50, dist)], dev)
+        per_call[str(B)] = round(t_all / (reps * layers) * 1e6, 2)
+        single[str(B)] = round(t_one / (reps * 10) * 1e6, 2)
+        gbs[str(B)] = round(B * seq_len * W.kv_bytes_per_token() / (t_all / (reps * layers)) / 1e9, 1)
+        del g_all, g_one, inp
+        torch.cuda.empty_cache()
+    return {"seq_len": seq_len, "us_per_call_in_layer_graph": per_call,
+            "us_per_single_call_graph_replay": single, "kv_read_gbs_in_layer_graph": gbs,
+            "layers_per_graph": layers}
+
+
 def run_decode_buckets(pa, args, dev, dist, world, rank):
-    """Decode-step latency by batch bucket, the way a serving engine replays one CUDA graph per
-    bucket and token: 1, 2, 4, 8, 16 and 32 sequences of 1,000 cached tokens (80 s of audio
-    each; one sequence is the single-stream decode configuration). Reports microseconds per
-    replay of the decode call (split kernel + merge) and the KV read rate at each bucket."""
-    buckets = (1, 2, 4, 8, 16, 32)
-    L = 1000
-    reps = max(args.steps, 1) * 200      # each replay is microseconds long
-    lat, gbs = {}, {}
+    """Decode-step latency by batch bucket (see bucket_latencies). The one-sequence bucket is
+    the single-stream decode configuration."""
     sampler = ClockSampler(args.clocks_out)
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
-    for B in buckets:
-        seed = W.CONFIG_SEED["decode_b1_l1000"]
-        inp = (W.make_workload("decode_b1_l1000", device=dev) if B == 1 else
-               W.make_paged(seed + B, np.full(B, L), np.ones(B, np.int64), device=dev))
-        out = torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
-        lse = torch.empty(B, W.HQ, dtype=torch.float32, device=dev)
-        ws = torch.empty(pa.decode_workspace_size(B, L), dtype=torch.uint8, device=dev)
-        call = lambda: pa.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0],
-                                            inp.block_table, inp.seq_lens, L, inp.scale,
-                                            out=out, lse=lse, workspace=ws)
-        call()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            call()
-        (t,) = max_over_ranks(dist, [timed_replays(g, reps, max(args.warmup, 0) * 20, dist)], dev)
-        lat[str(B)] = round(t / reps * 1e6, 2)
-        gbs[str(B)] = round(B * L * W.kv_bytes_per_token() / (t / reps) / 1e9, 1)
-        del g
+    res = bucket_latencies(pa, dev, dist, args.warmup)
     clocks = sampler.stop(device_uuid()) if rank == 0 else None
     hbm, bf16, bf16s, peak_src = peaks()
+    lat = res["us_per_call_in_layer_graph"]
+    g32 = res["kv_read_gbs_in_layer_graph"]["32"]
     if rank == 0:
         print(json.dumps({
-            "metric": "decode step latency by batch bucket (CUDA-graph replay), us", "value": lat["1"],
-            "unit": "us", "n_gpus": world, "steps": reps, "warmup": max(args.warmup, 0) * 20,
+            "metric": "decode latency by batch bucket (CUDA-graph replay), us per call", "value": lat["1"],
+            "unit": "us", "n_gpus": world, "steps": 200, "warmup": max(args.warmup, 3) * 5,
             "ms_per_step": round(lat["1"] / 1e3, 5), "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "decode_graph_buckets", "seq_len": L, "buckets": list(buckets),
-                       "timing": "CUDA events around back-to-back replays of one graph per bucket"},
-            "latency_us": lat, "kv_read_gbs": gbs,
+            "config": {"workload": "decode_graph_buckets", "seq_len": res["seq_len"], "buckets": list(BUCKETS),
+                       "timing": "CUDA events around back-to-back replays of a 28-call graph (one call per "
+                                 "layer) and of a one-call graph, per bucket"},
+            "buckets": res,
             "roofline": {"kernel": "attn_decode_paged (decode_splitkv + merge)", "bound": "hbm",
-                         "achieved": gbs["32"], "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs["32"] / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
+                         "achieved": g32, "peak": hbm, "unit": "GB/s",
+                         "frac": round(g32 / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
                          "traffic": None, "note": "at the 32-sequence bucket; small buckets are latency-bound"},
-            "gpu_launches": 2 * reps * len(buckets), "clocks": clocks}), flush=True)
+            "gpu_launches": 2 * 200 * (28 + 10) * len(BUCKETS), "clocks": clocks}), flush=True)
 
 
 def run_reference(args, world, rank):

@@ -23,6 +23,8 @@ prefill_4096_at_61440  one 4,096-query chunk at offset 61,440 (the last chunk of
 mixed_28l              28 layers, each with its own K/V pools: one 4,096-query chunk at
                        offset 32,768 plus 31 decode sequences with lengths uniform in
                        [5,000, 90,000]; the new tokens are appended before attention
+prefill_4096_at_32768  the prefill launch of one mixed_28l layer on its own (a 4,096-query
+                       chunk at offset 32,768): a small case for memory-traffic counters
 =====================  =============================================================
 
 Recipe: sequence lengths and page permutations come from numpy ``PCG64(seed)``; tensor
@@ -51,6 +53,7 @@ CONFIG_SEED = {
     "decode_ragged_b64": 1003,
     "prefill_4096_at_61440": 1004,
     "mixed_28l": 1005,
+    "prefill_4096_at_32768": 1008,
 }
 
 
@@ -202,6 +205,8 @@ def lengths_for(name: str, seed: int | None = None):
         return L, np.ones(64, dtype=np.int64)
     if name == "prefill_4096_at_61440":
         return np.array([61_440 + 4096]), np.array([4096])
+    if name == "prefill_4096_at_32768":
+        return np.array([32_768 + 4096]), np.array([4096])
     if name == "mixed_28l":
         L = rng.integers(5_000, 90_000, size=31, endpoint=True)
         return np.concatenate([[32_768 + 4096], L]), np.concatenate([[4096], np.ones(31, np.int64)])
