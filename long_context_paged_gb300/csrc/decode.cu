@@ -161,8 +161,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
     }
     fence_mbar_init();
   }
-  // the merge kernel only reads this grid's results after griddepcontrol.wait (full completion),
-  // so it may be launched as soon as every CTA of this grid has started
+  // This kernel is launched as a programmatic dependent of whatever precedes it on the stream,
+  // so its launch and the barrier set-up above overlap the tail of that kernel; nothing written
+  // by earlier work is read before this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the merge kernel only reads this grid's results after its own griddepcontrol.wait (full
+  // completion), so it may be launched as soon as every CTA of this grid has got here (the
+  // lengths it reads before that wait are final by now)
   asm volatile("griddepcontrol.launch_dependents;");
   build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
 
@@ -466,15 +471,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
 // split kernel is still running and wait (griddepcontrol.wait) until that grid has completed
 // and its writes are visible, which hides this launch behind the split kernel.
 constexpr int kMergeWarpsSmall = 16, kMergeWarpsLarge = 4;
+constexpr int kMergePrefixBatch = 64;  // batches this small: page range computed before the wait
 template <int kWarps>
 __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel on the stream may launch now; it waits for this grid before reading anything
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float red_m[kWarps], red_w[kWarps];
   __shared__ float4 red_o[kWarps][32];
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = p.hq, slots = p.stage_pages;
-  const int p0 = p.ws_prefix[b], p1 = p.ws_prefix[b + 1];
+  // For a small batch every warp computes this sequence's page range and the split's range size
+  // from the lengths, with the split kernel's own arithmetic, while the split kernel still runs;
+  // a large batch reads them from the workspace after the wait.
+  int p0 = 0, p1 = 0, W = 0;
+  const bool early = p.batch <= kMergePrefixBatch;
+  if (early) {
+    const int n0 = lane < p.batch ? (clamp_len(p, lane, false) + kPage - 1) / kPage : 0;
+    const int n1 = lane + 32 < p.batch ? (clamp_len(p, lane + 32, false) + kPage - 1) / kPage : 0;
+    int before = (lane < b ? n0 : 0) + (lane + 32 < b ? n1 : 0), total = n0 + n1;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    const int mine = b < 32 ? __shfl_sync(0xffffffffu, n0, b) : __shfl_sync(0xffffffffu, n1, b - 32);
+    p0 = before;
+    p1 = before + mine;
+    const int base = p.split_pages > 0 ? p.split_pages : kMinPagesPerCta;
+    W = max((total + p.max_ranges - 1) / p.max_ranges, base);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!early) {
+    p0 = p.ws_prefix[b];
+    p1 = p.ws_prefix[b + 1];
+  }
   uint16_t* orow = p.out + (static_cast<int64_t>(b) * hq + h) * kHeadDim + 4 * lane;
   if (p1 == p0) {
     if (warp == 0) {
@@ -483,7 +514,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
     }
     return;
   }
-  const int W = p.ws_header[0];
+  if (!early) W = p.ws_header[0];
   const int r0 = p0 / W, r1 = (p1 - 1) / W;
   if (r0 == r1 && slots == 1) return;  // finished inside one CTA
   // partials c0 .. c1: record b * slots + c, c = range * slots + page slot
@@ -705,13 +736,28 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   p.starve = g_debug_starve ? 1 : 0;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  switch (hkv) {
-    case 8: decode_splitkv_kernel<8><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
-    case 4: decode_splitkv_kernel<4><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
-    case 2: decode_splitkv_kernel<2><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
-    default: decode_splitkv_kernel<1><<<plan.grid, kThreads, sizeof(DecodeSmem), st>>>(p); break;
+  {
+    // a programmatic dependent of the previous work on the stream: it may launch during that
+    // work's tail and waits (griddepcontrol.wait) before reading any input
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(DecodeSmem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    switch (hkv) {
+      case 8: e = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<8>, p); break;
+      case 4: e = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<4>, p); break;
+      case 2: e = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<2>, p); break;
+      default: e = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<1>, p); break;
+    }
+    if (e != cudaSuccess) return record_cuda_error(e, "decode_splitkv_kernel");
   }
-  PA_CHECK_LAUNCH("decode_splitkv_kernel");
   {
     cudaLaunchConfig_t cfg = {};
     // partials per sequence when the lengths are equal: ceil(ranges / batch), plus one for a
