@@ -67,6 +67,7 @@ typedef enum pa_status {
 #define PA_DEV_ERR_PAGE_OOB 1u /* a block-table entry needed by the call was not in [0, num_pages) */
 #define PA_DEV_ERR_LENGTH 2u   /* a length did not fit: seq_len < 0 or > bt_stride*16, q_len > seq_len, ... */
 #define PA_DEV_ERR_TIMEOUT 4u  /* a bounded wait inside a kernel gave up (the kernel returned early) */
+#define PA_DEV_ERR_INTERNAL 8u /* a kernel found the GPU's layout not as built for (it did nothing) */
 
 typedef struct pa_dims {
   int32_t num_q_heads;  /* Hq  (16) */

@@ -23,12 +23,13 @@ __all__ = [
     "kv_append_paged", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_prefill_chunk",
     "attn_merge_lse", "adaptor_mlp_merge4", "adaptor_workspace_size",
     "decode_workspace_size", "prefill_workspace_size", "read_device_status", "debug_decode_starve",
-    "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "lib_path",
+    "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "DEV_ERR_INTERNAL", "lib_path",
 ]
 
 DEV_ERR_PAGE_OOB = 1
 DEV_ERR_LENGTH = 2
 DEV_ERR_TIMEOUT = 4
+DEV_ERR_INTERNAL = 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None

@@ -25,8 +25,10 @@
 //   O_t += P_t V_j          tcgen05.mma, A = P_t (TMEM), B = V_j (smem, MN-major), D = O_t
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 // Warp roles: 0-3 softmax of M tile 0, 4-7 softmax of M tile 1, 8 TMA producer of V, 9 MMA
-// issuer, 10 TMA producer of Q and K, 11 idle (it completes the third warpgroup, which gives
-// its registers to the softmax).
+// issuer, 10 TMA producer of Q and K, 11 scheduler: it alone walks the work split and publishes
+// each piece (job, key-tile range) in a small shared-memory ring, so the other roles hold only
+// the few fields they use instead of the walker's state (registers are what bounds the
+// softmax and the issuer).
 // K/V tiles arrive by tiled TMA straight from the page pools: one 16-token page x 64 dims per
 // copy (a 3-D tensor map over [tokens][kv heads][dims] with 128-byte swizzle), so the block
 // table is applied per page without a gather pass. Pages past the sequence are fetched at an
@@ -59,6 +61,9 @@ constexpr int kThreads = 384; // 8 softmax warps + producer + MMA + 2 spare (3 w
 constexpr int kProducerWarp = 8;   // V tiles
 constexpr int kMmaWarp = 9;
 constexpr int kKProducerWarp = 10; // Q and K tiles
+constexpr int kSchedWarp = 11;      // walks the work split and publishes the pieces
+constexpr int kPieceRing = 4;       // published pieces in flight
+constexpr int kPieceReaders = 11;   // warps that read every piece: 8 softmax, 2 producers, MMA
 constexpr uint32_t kBlockBytes = 128 * 128;  // 128 rows x 64 bf16 (one swizzled 64-dim block)
 constexpr uint32_t kTileBytes = 2 * kBlockBytes;
 constexpr float kRescaleThreshold = 8.0f;
@@ -69,16 +74,24 @@ constexpr int kVStages = 3;   // V is needed a whole P*V later than K: one more 
 // work split each job occupies its key tiles followed by this many cost units, so that a CTA whose
 // share holds many short jobs is not overloaded; the cost units hold no key tile.
 constexpr int kJobCost = 3;
-// Register split: the two softmax warpgroups grow to 200 registers per thread, the
-// producer/MMA warpgroup shrinks to 104 (at 72 the issuer's loop spilled and starved the tensor
-// pipe; softmax below ~200 spills); 256 * 200 + 128 * 104 = 64,512 = 384 threads x 168, the
-// budget the CTA is launched with (checked on the host before every launch).
-constexpr int kSoftmaxRegs = 200;
-constexpr int kControlRegs = 104;
+// Register split: the two softmax warpgroups grow to 208 registers per thread, the
+// producer/MMA/scheduler warpgroup shrinks to 88 (measured: 200/104 about 1 % slower, 216/72
+// and 192/120 7-9 % slower: the issuer's loop and the softmax both stall when they spill);
+// 256 * 208 + 128 * 88 = 64,512 = 384 threads x 168, the budget the CTA is launched with
+// (checked on the host before every launch).
+constexpr int kSoftmaxRegs = 208;
+constexpr int kControlRegs = 88;
 constexpr int kLaunchRegs = (256 * kSoftmaxRegs + 128 * kControlRegs) / kThreads;
 // A partial result: o [2 heads][128 rows][128] fp32, then lse [2][128] fp32.
 constexpr size_t kRecordO = 2 * 128 * 128 * sizeof(float);
 constexpr size_t kRecordBytes = kRecordO + 2 * 128 * sizeof(float);
+
+// One piece of the walk as the roles use it: key tiles [jb, je) of job (b, g, qt), with the
+// chunk's first packed row q0, its length n, the sequence's keys L and the chunk's offset off;
+// J = the job's key tiles; valid = 0 ends the walk.
+struct PieceDesc {
+  int32_t b, g, qt, q0, n, L, off, J, jb, je, valid;
+};
 
 struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
   uint8_t q[2][2][kBlockBytes];   // [M tile][64-dim block]
@@ -93,6 +106,8 @@ struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
   uint64_t s_full[2], p1_full, o_ready[2], o_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
+  PieceDesc piece[kPieceRing];
+  uint64_t piece_full[kPieceRing], piece_empty[kPieceRing];
   long long warp_sums[kThreads / 32];
   long long total_units;
   long long unit_prefix[kMaxBatch + 1];  // first unit of each sequence
@@ -102,7 +117,9 @@ struct PrefillTcSmem {  // placed at a 1024-byte aligned address (swizzle atoms)
   long long plan_u0, plan_u1;            // this CTA's range of the remaining units
 };
 
-static_assert(sizeof(PrefillTcSmem) + 1024 <= 232448, "prefill shared memory over the 227 KB limit");
+// The dynamic shared memory of a CTA starts 1024-byte aligned on this GPU (after the 1 KB the
+// system reserves per block), which the swizzled operand tiles need; the kernel checks it.
+static_assert(sizeof(PrefillTcSmem) <= 232448, "prefill shared memory over the 227 KB limit");
 
 struct PrefillTcParams {
   int32_t hkv, hq;        // KV heads and query heads of the call (hq = 2 hkv)
@@ -289,6 +306,23 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int
   return false;
 }
 
+// The next published piece, read by a whole warp: wait for its slot, copy it, release the slot.
+// A wait that gives up ends the walk (valid = 0) after flagging PA_DEV_ERR_TIMEOUT.
+__device__ __forceinline__ PieceDesc take_piece_warp(PrefillTcSmem& s, uint32_t& k, int lane,
+                                                     int32_t* status) {
+  const uint32_t slot = k % kPieceRing, ph = (k / kPieceRing) & 1;
+  PieceDesc d;
+  if (!__all_sync(0xffffffffu, wait_or_flag(&s.piece_full[slot], ph, status))) {
+    d.valid = 0;
+    return d;
+  }
+  d = s.piece[slot];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&s.piece_empty[slot]);
+  ++k;
+  return d;
+}
+
 __device__ __forceinline__ long long warp_incl_scan64(long long v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -434,11 +468,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map, const PrefillTcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  PrefillTcSmem& s = *reinterpret_cast<PrefillTcSmem*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
   asm volatile("griddepcontrol.launch_dependents;");  // the merge kernel waits for completion
+  if ((smem_addr(smem_raw) & 1023u) != 0) {
+    // not the layout this kernel was built for: do nothing, and make the merge do nothing
+    // (it skips every job below ws_header[3])
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      p.ws_header[3] = 0x7fffffffffffffffll;
+      flag_error(p.status, PA_DEV_ERR_INTERNAL);
+    }
+    return;
+  }
+  PrefillTcSmem& s = *reinterpret_cast<PrefillTcSmem*>(smem_raw);
   build_unit_prefix(p, s);
   const long long total = s.total_units;
   const int G = gridDim.x;
@@ -475,6 +516,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     }
     mbar_init(&s.p1_full, 4);         // one arrive per softmax-1 warp
     mbar_init(&s.mma_done, 1);
+    for (int i = 0; i < kPieceRing; ++i) {
+      mbar_init(&s.piece_full[i], 1);
+      mbar_init(&s.piece_empty[i], kPieceReaders);
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tc::tmem_alloc<512>(&s.tmem_base);
@@ -483,8 +528,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
 
-  JobWalker jw;
-  jw.start(p, s.unit_prefix, s.job_prefix, rounds, G, U0, U1);
 
   if (warp >= 8) {
     tc::regs_decrease<kControlRegs>();
@@ -500,14 +543,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     uint64_t* empty = is_k ? s.k_empty : s.v_empty;
     const int oob_token = static_cast<int>(p.num_pages * kPage);  // zero-filled coordinate
     bool ok = true;
-    uint32_t it = 0, jc = 0;
-    for (; jw.cur.valid && ok; jw.next()) {
-      const Piece& pc = jw.cur;
+    uint32_t it = 0, jc = 0, pk = 0;
+    for (PieceDesc pc = take_piece_warp(s, pk, lane, p.status); pc.valid && ok;
+         pc = take_piece_warp(s, pk, lane, p.status)) {
       const int32_t* bt_row = p.block_table + static_cast<int64_t>(pc.b) * p.bt_stride;
       auto page_token = [&](int j) {
         int tok = oob_token;
         const int key0 = j * kTileN + kPage * lane;
-        if (lane < kTileN / kPage && key0 < pc.s.L) {
+        if (lane < kTileN / kPage && key0 < pc.L) {
           const int e = bt_row[key0 / kPage];
           if (e < 0 || e >= p.num_pages) {
             flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
@@ -526,7 +569,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             for (int t = 0; t < 2; ++t)
               for (int kb = 0; kb < 2; ++kb)
                 tc::tma_load_3d(s.q[t][kb], &q_map, kb * 64, 2 * pc.g + t,
-                                pc.s.q0 + pc.qt * kTileM, &s.q_full);
+                                pc.q0 + pc.qt * kTileM, &s.q_full);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -602,13 +645,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       uint32_t tph = 0;              // parity of the current tile's S / P phases
       bool ok = true;
       uint32_t jc = 0;
-      for (; jw.cur.valid && ok; jw.next(), ++jc) {
-        const int nt = jw.cur.je - jw.cur.jb;
+      uint32_t pk = 0;
+      for (;; ++jc) {
+        // the next piece: only its tile count and the sequence end are needed here
+        const uint32_t pslot = pk % kPieceRing;
+        if (!wait_or_flag(&s.piece_full[pslot], (pk / kPieceRing) & 1, p.status)) break;
+        const volatile PieceDesc& pv = s.piece[pslot];
+        const int pvalid = pv.valid, pjb = pv.jb, pje = pv.je, pL = pv.L;
+        mbar_arrive(&s.piece_empty[pslot]);
+        ++pk;
+        if (!pvalid || !ok) break;
+        const int nt = pje - pjb;
         // The piece's last tile runs past the sequence end when L < je * 128. Its page that
         // holds key L - 1 was loaded whole, so the V rows of the pool slots after the last key
         // ([zl, next multiple of 16)) are zeroed, that P = 0 there cannot meet an unwritten
         // (possibly NaN) slot; the pages after it were never loaded (zero fill).
-        const int zl = jw.cur.s.L - (jw.cur.je - 1) * kTileN;
+        const int zl = pL - (pje - 1) * kTileN;
         const int zero_i = (zl > 0 && zl < kTileN && (zl & 15) != 0) ? nt - 1 : -1;
         const uint32_t qph = jc & 1, oph = (jc - 1) & 1;
         ok = wait_or_flag(&s.q_full, qph, p.status) && wait_or_flag(&s.k_full[kst], kph, p.status);
@@ -677,6 +729,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       wait_or_flag(&s.mma_done, 0, p.status);
     }
     __syncwarp();
+  } else if (warp == kSchedWarp) {
+    // ------------------------------------------------------------------ scheduler
+    if (lane == 0) {
+      JobWalker jw;
+      jw.start(p, s.unit_prefix, s.job_prefix, rounds, G, U0, U1);
+      for (uint32_t k = 0;; ++k) {
+        const uint32_t slot = k % kPieceRing, ph = (k / kPieceRing) & 1;
+        if (!wait_or_flag(&s.piece_empty[slot], ph ^ 1u, p.status)) break;
+        const Piece& c = jw.cur;
+        PieceDesc d;
+        d.b = c.b;
+        d.g = c.g;
+        d.qt = c.qt;
+        d.q0 = c.s.q0;
+        d.n = c.s.n;
+        d.L = c.s.L;
+        d.off = c.s.off;
+        d.J = c.J;
+        d.jb = c.jb;
+        d.je = c.je;
+        d.valid = c.valid ? 1 : 0;
+        s.piece[slot] = d;
+        mbar_arrive(&s.piece_full[slot]);  // release: the readers' waits make d visible
+        if (!c.valid) break;
+        jw.next();
+      }
+    }
+    __syncwarp();
   }
   } else {
     tc::regs_increase<kSoftmaxRegs>();
@@ -691,11 +771,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     bool ok = true;
     uint32_t it = 0, jcs = 0;
     const bool leader = quarter == 0 && lane == 0;  // releases stages for this M tile
-    for (; jw.cur.valid && ok; jw.next(), ++jcs) {
-      const Piece& pc = jw.cur;
-      const int nt = pc.je - pc.jb;
-      const int qrow = pc.qt * kTileM + r;
-      const int qpos = pc.s.off + qrow;            // absolute position of this query
+    uint32_t pk = 0;
+    for (;; ++jcs) {
+      // the next piece; its slot is held until the epilogue, which reads the rest of it
+      const uint32_t pslot = pk % kPieceRing;
+      if (!__all_sync(0xffffffffu, wait_or_flag(&s.piece_full[pslot], (pk / kPieceRing) & 1, p.status)))
+        break;
+      const volatile PieceDesc& pv = s.piece[pslot];
+      if (!pv.valid || !ok) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.piece_empty[pslot]);
+        break;
+      }
+      const int pjb = pv.jb;
+      const int nt = pv.je - pjb;
+      const int qrow = pv.qt * kTileM + r;
+      const int qpos = pv.off + qrow;              // absolute position of this query
       float m_used = -CUDART_INF_F, l = 0.f;
       for (int i = 0; i < nt; ++i) {
         const uint32_t cur = it + i;
@@ -715,7 +806,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         for (int c = 0; c < 4; ++c)
           tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sb + c * 32));
         tc::tmem_wait_ld();
-        const int k0 = (pc.jb + i) * kTileN;
+        const int k0 = (pjb + i) * kTileN;
         if (k0 + kTileN - 1 > qpos) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -797,12 +888,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       if (!ok) break;
       tc::fence_after_sync();
       if (leader) mbar_arrive(&s.v_empty[(it + nt - 1) % kVStages]);
-      const bool live = qrow < pc.s.n;
+      const int pn = pv.n, pq0 = pv.q0, pJ = pv.J, pg = pv.g;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.piece_empty[pslot]);
+      ++pk;
+      const bool live = qrow < pn;
       const float inv = 1.0f / l;
-      const bool whole = pc.jb == 0 && pc.je == pc.J;
-      const int head = 2 * pc.g + t;
+      const bool whole = pjb == 0 && pjb + nt == pJ;
+      const int head = 2 * pg + t;
       if (whole) {
-        uint16_t* dst = p.out + (static_cast<int64_t>(pc.s.q0 + qrow) * p.hq + head) * kHeadDim;
+        uint16_t* dst = p.out + (static_cast<int64_t>(pq0 + qrow) * p.hq + head) * kHeadDim;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o32[32];
@@ -821,11 +916,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           }
         }
         if (live && p.lse != nullptr)
-          p.lse[static_cast<int64_t>(pc.s.q0 + qrow) * p.hq + head] = (m_used + log2f(l)) * kLn2;
+          p.lse[static_cast<int64_t>(pq0 + qrow) * p.hq + head] = (m_used + log2f(l)) * kLn2;
       } else {
         // a piece of a job shared with neighbouring CTAs: slot 1 if it starts the job, else 0.
         // A row that saw no key in this piece contributes nothing: o = 0, lse = -inf.
-        const int slot = pc.jb == 0 ? 1 : 0;
+        const int slot = pjb == 0 ? 1 : 0;
         const bool empty = m_used == -CUDART_INF_F;
         const float sc_o = empty ? 0.f : inv;
         uint8_t* rec = p.ws_records + (2 * static_cast<size_t>(blockIdx.x) + slot) * kRecordBytes;
@@ -990,7 +1085,7 @@ pa_status launch_prefill_tc(int32_t hkv, const void* q, int32_t total_q, const i
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
-  const int smem = static_cast<int>(sizeof(PrefillTcSmem)) + 1024;
+  const int smem = static_cast<int>(sizeof(PrefillTcSmem));
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

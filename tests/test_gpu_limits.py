@@ -35,6 +35,26 @@ def test_decode_batch_of_4096(cuda_lib):
     check_attn(out, lse, ref_o, ref_l, rows=seqs, what="4,096 sequences (sampled)")
 
 
+@pytest.mark.parametrize("split", [16, 4096])
+def test_decode_batch_of_4096_with_a_split_size(cuda_lib, split):
+    """A split of one page per range would need more ranges than the workspace holds (64 per
+    SM); the range size is raised until it fits, and the result is unchanged. A large split puts
+    many short sequences into one range."""
+    rng = np.random.default_rng(65)
+    lens = rng.integers(0, 400, size=4096)
+    inp = W.make_paged(65, lens, np.ones(4096, np.int64), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = cuda_lib.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0],
+                                          inp.block_table, inp.seq_lens, 400, inp.scale,
+                                          split_tokens=split, status=status)
+    torch.cuda.synchronize()
+    assert cuda_lib.read_device_status(status) == 0
+    seqs = sorted(set(int(x) for x in rng.integers(0, 4096, 96)) | {0, 4095})
+    ref_o, ref_l = oracle.decode(bits(inp.q[0]), bits(inp.k_pools[0]), bits(inp.v_pools[0]),
+                                 inp.host_block_table, inp.host_seq_lens, inp.scale, seqs=seqs)
+    check_attn(out, lse, ref_o, ref_l, rows=seqs, what=f"4,096 sequences, split {split} (sampled)")
+
+
 def test_prefill_128_chunks_in_one_call(cuda_lib):
     rng = np.random.default_rng(62)
     q_lens = rng.integers(1, 40, size=128)
