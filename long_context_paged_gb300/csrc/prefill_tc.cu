@@ -82,7 +82,8 @@ constexpr int kJobCost = 3;
 constexpr int kSoftmaxRegs = 208;
 constexpr int kControlRegs = 88;
 constexpr int kLaunchRegs = (256 * kSoftmaxRegs + 128 * kControlRegs) / kThreads;
-// A partial result: o [2 heads][128 rows][128] fp32, then lse [2][128] fp32.
+// A partial result: o [2 heads][32 float4 columns][128 rows] (16-byte units; consecutive rows
+// are adjacent, so a warp's 32 rows store and load 512 contiguous bytes), then lse [2][128] fp32.
 constexpr size_t kRecordO = 2 * 128 * 128 * sizeof(float);
 constexpr size_t kRecordBytes = kRecordO + 2 * 128 * sizeof(float);
 
@@ -924,7 +925,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const bool empty = m_used == -CUDART_INF_F;
         const float sc_o = empty ? 0.f : inv;
         uint8_t* rec = p.ws_records + (2 * static_cast<size_t>(blockIdx.x) + slot) * kRecordBytes;
-        float* dst = reinterpret_cast<float*>(rec) + (t * 128 + r) * kHeadDim;
+        float4* dst = reinterpret_cast<float4*>(rec) + t * 32 * 128 + r;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o32[32];
@@ -932,7 +933,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
           tc::tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            reinterpret_cast<float4*>(dst + c * 32)[k] =
+            dst[(c * 8 + k) * 128] =
                 make_float4(__uint_as_float(o32[4 * k]) * sc_o, __uint_as_float(o32[4 * k + 1]) * sc_o,
                             __uint_as_float(o32[4 * k + 2]) * sc_o, __uint_as_float(o32[4 * k + 3]) * sc_o);
         }
@@ -1002,10 +1003,10 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
     if (lp == -CUDART_INF_F) continue;  // the piece held no key visible to this row
     const float w = fast_exp2((lp - m) * kLog2e);
     sum += w;
-    const float4* o = reinterpret_cast<const float4*>(rec) + (t * 128 + r) * (kHeadDim / 4);
+    const float4* o = reinterpret_cast<const float4*>(rec) + t * 32 * 128 + r;
 #pragma unroll
     for (int d = 0; d < kHeadDim / 4; ++d) {
-      const float4 v = o[d];
+      const float4 v = o[d * 128];
       acc[4 * d] += w * v.x;
       acc[4 * d + 1] += w * v.y;
       acc[4 * d + 2] += w * v.z;
