@@ -44,10 +44,9 @@ constexpr int kStages = 3;
 constexpr uint32_t kStageBytes = kPage * kHkv * kHeadDim * 2;
 constexpr int kMaxBatch = 4096;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-#ifndef PA_DECODE_MIN_PAGES
-#define PA_DECODE_MIN_PAGES 1
-#endif
-constexpr int kMinPagesPerCta = PA_DECODE_MIN_PAGES;
+// Fewest pages per range by default: a short batch is spread one page per SM (two or four
+// pages per CTA measured 0.9 and 2.4-2.9 us slower for one sequence of 1,000 keys).
+constexpr int kMinPagesPerCta = 1;
 
 struct DecodeSmem {
   uint8_t kv[kStages][2][kStageBytes];
