@@ -25,6 +25,13 @@ mixed_28l              28 layers, each with its own K/V pools: one 4,096-query c
                        [5,000, 90,000]; the new tokens are appended before attention
 prefill_4096_at_32768  the prefill launch of one mixed_28l layer on its own (a 4,096-query
                        chunk at offset 32,768): a small case for memory-traffic counters
+prefill_ragged_mix     one prefill call over six requests (RAGGED_PREFILL_MIX): chunks of
+                       4,096 / 2,048 / 1,024 / 512 queries at offsets 28,672 / 61,440 /
+                       10,000 / 0 and extends of 1 and 2 tokens after 5,000 and 20,000
+decode_graph_buckets   batches of 1, 2, 4, 8, 16 and 32 sequences of 1,000 tokens, 28
+                       layers with their own pools (CUDA-graph replay latency)
+adaptor_90min          270,000 encoder frames (90 minutes) through the 4x merge and the
+                       adaptor MLP (make_adaptor)
 =====================  =============================================================
 
 Recipe: sequence lengths and page permutations come from numpy ``PCG64(seed)``; tensor
