@@ -135,6 +135,51 @@ def _check(call, code):
         raise PagedAttnError(call, code)
 
 
+def _on_device(call, *tensors):
+    """Every tensor must live on the current CUDA device: the library launches there, and a
+    pointer into another GPU's memory would be read by the wrong device."""
+    dev = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and t.device.index != dev:
+            raise ValueError(f"{call}: tensors must be on the current CUDA device (cuda:{dev}), "
+                             f"got {t.device}")
+
+
+def _shape(name, t, shape):
+    """t must have this shape (None entries match anything)."""
+    if t.dim() != len(shape) or any(w is not None and d != w for d, w in zip(t.shape, shape)):
+        raise ValueError(f"{name} must have shape {tuple('*' if w is None else w for w in shape)}, "
+                         f"got {tuple(t.shape)}")
+
+
+def _rows_at_least(name, t, n):
+    if t.shape[0] < n:
+        raise ValueError(f"{name} must have at least {n} rows, got {t.shape[0]}")
+
+
+def _heads(dims):
+    """(query heads, KV heads) of a shape the library supports, else None: the library itself
+    then rejects the call (PA_ERR_UNSUPPORTED) and the shape checks below are skipped."""
+    d = _dims(dims)
+    if (d.head_dim == 128 and d.page_size == 16 and d.num_kv_heads in (1, 2, 4, 8)
+            and d.num_q_heads == 2 * d.num_kv_heads):
+        return d.num_q_heads, d.num_kv_heads
+    return None
+
+
+def _pools(k_pool, v_pool, hkv):
+    _shape("k_pool", k_pool, (None, 16, hkv, 128))
+    _shape("v_pool", v_pool, tuple(k_pool.shape))
+
+
+def _given(t, name, dtype, shape):
+    """A caller-provided output buffer: dtype, layout and shape checked, since the kernels write
+    every element of it."""
+    if t is not None:
+        _need(t, name, dtype)
+        _shape(name, t, shape)
+
+
 # ----------------------------------------------------------------------------------------------
 # the four calls
 # ----------------------------------------------------------------------------------------------
@@ -146,6 +191,18 @@ def kv_append_paged(k_new, v_new, cu_new_lens, start_pos, block_table, k_pool, v
                     (block_table, "block_table", torch.int32), (k_pool, "k_pool", torch.bfloat16),
                     (v_pool, "v_pool", torch.bfloat16)):
         _need(t, n, d)
+    B = start_pos.shape[0]
+    _rows_at_least("cu_new_lens", cu_new_lens, B + 1)
+    _rows_at_least("block_table", block_table, B)
+    heads = _heads(dims)
+    if heads is not None:
+        _shape("k_new", k_new, (None, heads[1], 128))
+        _shape("v_new", v_new, tuple(k_new.shape))
+        _pools(k_pool, v_pool, heads[1])
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _on_device("kv_append_paged", k_new, v_new, cu_new_lens, start_pos, block_table, k_pool,
+               v_pool, status)
     lib = load()
     _check("kv_append_paged", lib.kv_append_paged(
         _dims(dims), _ptr(k_new), _ptr(v_new), k_new.shape[0], _ptr(cu_new_lens), _ptr(start_pos),
@@ -179,12 +236,24 @@ def attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int
     _need(block_table, "block_table", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     B = q.shape[0]
+    _rows_at_least("block_table", block_table, B)
+    _rows_at_least("seq_lens", seq_lens, B)
+    heads = _heads(dims)
+    if heads is not None:
+        _shape("q", q, (B, heads[0], 128))
+        _pools(k_pool, v_pool, heads[1])
+        _given(out, "out", torch.bfloat16, (B, heads[0], 128))
+        _given(lse, "lse", torch.float32, (B, heads[0]))
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty(B, q.shape[1], dtype=torch.float32, device=q.device)
     ws_bytes = decode_workspace_size(B, max_seq_len, split_tokens, dims)
     workspace = _workspace(ws_bytes, q.device, workspace)
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _on_device("attn_decode_paged", q, k_pool, v_pool, block_table, seq_lens, out, lse,
+               workspace, status)
     lib = load()
     _check("attn_decode_paged", lib.attn_decode_paged(
         _dims(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
@@ -208,6 +277,19 @@ def attn_decode_paged_noalloc(q, k_pool, v_pool, block_table, seq_lens, max_seq_
     _need(block_table, "block_table", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     _need(out, "out", torch.bfloat16, 3)
+    B = q.shape[0]
+    _rows_at_least("block_table", block_table, B)
+    _rows_at_least("seq_lens", seq_lens, B)
+    heads = _heads(dims)
+    if heads is not None:
+        _shape("q", q, (B, heads[0], 128))
+        _pools(k_pool, v_pool, heads[1])
+        _given(out, "out", torch.bfloat16, (B, heads[0], 128))
+        _given(lse, "lse", torch.float32, (B, heads[0]))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _on_device("attn_decode_paged_noalloc", q, k_pool, v_pool, block_table, seq_lens, out, lse,
+               status)
     lib = load()
     _check("attn_decode_paged_noalloc", lib.attn_decode_paged_noalloc(
         _dims(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
@@ -227,6 +309,15 @@ def attn_prefill_chunk(q, cu_q_lens, k_pool, v_pool, block_table, seq_lens, max_
     _need(block_table, "block_table", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     B = seq_lens.shape[0]
+    Tq = q.shape[0]
+    _rows_at_least("cu_q_lens", cu_q_lens, B + 1)
+    _rows_at_least("block_table", block_table, B)
+    heads = _heads(dims)
+    if heads is not None:
+        _shape("q", q, (Tq, heads[0], 128))
+        _pools(k_pool, v_pool, heads[1])
+        _given(out, "out", torch.bfloat16, (Tq, heads[0], 128))
+        _given(lse, "lse", torch.float32, (Tq, heads[0]))
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
@@ -234,6 +325,10 @@ def attn_prefill_chunk(q, cu_q_lens, k_pool, v_pool, block_table, seq_lens, max_
     ws_bytes = prefill_workspace_size(B, max_q_len, max_seq_len, dims)
     if ws_bytes > 0:
         workspace = _workspace(ws_bytes, q.device, workspace)
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _on_device("attn_prefill_chunk", q, cu_q_lens, k_pool, v_pool, block_table, seq_lens, out,
+               lse, workspace, status)
     lib = load()
     _check("attn_prefill_chunk", lib.attn_prefill_chunk(
         _dims(dims), _ptr(q), _ptr(cu_q_lens), q.shape[0], _ptr(k_pool), _ptr(v_pool),
@@ -249,10 +344,14 @@ def attn_merge_lse(o_parts, lse_parts, *, out=None, lse_out=None, stream=None):
     _need(o_parts, "o_parts", torch.float32, 4)
     _need(lse_parts, "lse_parts", torch.float32, 3)
     S, R, H, D = o_parts.shape
+    _shape("lse_parts", lse_parts, (S, R, H))
+    _given(out, "out", torch.bfloat16, (R, H, D))
+    _given(lse_out, "lse_out", torch.float32, (R, H))
     if out is None:
         out = torch.empty(R, H, D, dtype=torch.bfloat16, device=o_parts.device)
     if lse_out is None:
         lse_out = torch.empty(R, H, dtype=torch.float32, device=o_parts.device)
+    _on_device("attn_merge_lse", o_parts, lse_parts, out, lse_out)
     lib = load()
     _check("attn_merge_lse", lib.attn_merge_lse(S, R, H, D, _ptr(o_parts), _ptr(lse_parts),
                                                 _ptr(out), _ptr(lse_out), _stream(stream)))
@@ -274,11 +373,20 @@ def adaptor_mlp_merge4(frames, w1, b1, w2, b2, gamma, beta, eps: float = 1e-5, *
         _need(t, n, torch.float32, 1)
     n_frames = frames.shape[0]
     T = n_frames // 4
+    _shape("frames", frames, (n_frames, 1024))
+    _shape("w1", w1, (1024, 4096))
+    _shape("w2", w2, (1024, 1024))
+    for t, n in ((b1, "b1"), (b2, "b2"), (gamma, "gamma"), (beta, "beta")):
+        _shape(n, t, (1024,))
+    _given(out, "out", torch.bfloat16, (T, 1024))
     if out is None:
         out = torch.empty(T, 1024, dtype=torch.bfloat16, device=frames.device)
     if workspace is None:
         workspace = torch.empty(max(256, adaptor_workspace_size(n_frames)), dtype=torch.uint8,
                                 device=frames.device)
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _on_device("adaptor_mlp_merge4", frames, w1, b1, w2, b2, gamma, beta, out, workspace, status)
     lib = load()
     _check("adaptor_mlp_merge4", lib.adaptor_mlp_merge4(
         n_frames, _ptr(frames), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), _ptr(gamma), _ptr(beta),

@@ -246,3 +246,29 @@ def test_decode_bounded_wait_gives_up_and_the_next_call_is_correct(cuda_lib):
     assert pa.read_device_status(status) == 0
     ref_o, ref_l = oracle_decode(inp)
     check_attn(out, lse, ref_o, ref_l, what="after the timed-out call")
+
+
+def test_binding_rejects_misshaped_buffers(cuda_lib):
+    """The binding checks shapes the library cannot see through raw pointers (a short block
+    table, a small output buffer, pools of the wrong head count) before anything is launched."""
+    pa = cuda_lib
+    inp = W.make_paged(17, [100, 200], [1, 1], device="cuda")
+    q, kp, vp = inp.q[0], inp.k_pools[0], inp.v_pools[0]
+    bad = [
+        dict(block_table=inp.block_table[:1]),
+        dict(seq_lens=inp.seq_lens[:1]),
+        dict(out=torch.empty(2, 16, 64, dtype=torch.bfloat16, device="cuda")),
+        dict(lse=torch.empty(2, 8, dtype=torch.float32, device="cuda")),
+        dict(k_pool=kp[:, :, :4].contiguous()),
+    ]
+    for kw in bad:
+        args = dict(block_table=inp.block_table, seq_lens=inp.seq_lens, k_pool=kp)
+        args.update({k: v for k, v in kw.items() if k in args})
+        extra = {k: v for k, v in kw.items() if k not in args}
+        with pytest.raises(ValueError):
+            pa.attn_decode_paged(q, args["k_pool"], vp, args["block_table"], args["seq_lens"],
+                                 200, inp.scale, **extra)
+    with pytest.raises(ValueError):
+        pa.attn_prefill_chunk(q, inp.cu_q_lens, kp, vp, inp.block_table, inp.seq_lens, 1, 200,
+                              inp.scale, out=torch.empty(1, 16, 128, dtype=torch.bfloat16,
+                                                         device="cuda"))
