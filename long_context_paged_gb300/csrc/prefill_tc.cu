@@ -899,11 +899,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       const int head = 2 * pg + t;
       if (whole) {
         uint16_t* dst = p.out + (static_cast<int64_t>(pq0 + qrow) * p.hq + head) * kHeadDim;
+        // all of O's 128 columns loaded at once (the scores' registers are free here), one wait
+        uint32_t oall[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(t_o + c * 32, oall[c]);
+        tc::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t o32[32];
-          tc::tmem_ld32(t_o + c * 32, o32);
-          tc::tmem_wait_ld();
+          const uint32_t (&o32)[32] = oall[c];
           if (live) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -926,11 +929,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const float sc_o = empty ? 0.f : inv;
         uint8_t* rec = p.ws_records + (2 * static_cast<size_t>(blockIdx.x) + slot) * kRecordBytes;
         float4* dst = reinterpret_cast<float4*>(rec) + t * 32 * 128 + r;
+        uint32_t oall[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(t_o + c * 32, oall[c]);
+        tc::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t o32[32];
-          tc::tmem_ld32(t_o + c * 32, o32);
-          tc::tmem_wait_ld();
+          const uint32_t (&o32)[32] = oall[c];
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             dst[(c * 8 + k) * 128] =
