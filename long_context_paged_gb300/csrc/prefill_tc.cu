@@ -897,13 +897,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
       const float inv = 1.0f / l;
       const bool whole = pjb == 0 && pjb + nt == pJ;
       const int head = 2 * pg + t;
+      // all of O's 128 columns loaded at once (the scores' registers are free here), one wait;
+      // O's TMEM columns are then released to the next piece's first P*V before the stores
+      uint32_t oall[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(t_o + c * 32, oall[c]);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.o_free[t]);
       if (whole) {
         uint16_t* dst = p.out + (static_cast<int64_t>(pq0 + qrow) * p.hq + head) * kHeadDim;
-        // all of O's 128 columns loaded at once (the scores' registers are free here), one wait
-        uint32_t oall[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32(t_o + c * 32, oall[c]);
-        tc::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t (&o32)[32] = oall[c];
@@ -929,10 +933,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const float sc_o = empty ? 0.f : inv;
         uint8_t* rec = p.ws_records + (2 * static_cast<size_t>(blockIdx.x) + slot) * kRecordBytes;
         float4* dst = reinterpret_cast<float4*>(rec) + t * 32 * 128 + r;
-        uint32_t oall[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32(t_o + c * 32, oall[c]);
-        tc::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t (&o32)[32] = oall[c];
@@ -945,9 +945,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         reinterpret_cast<float*>(rec + kRecordO)[t * 128 + r] =
             empty ? -CUDART_INF_F : (m_used + log2f(l)) * kLn2;
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.o_free[t]);
       it += nt;
     }
   }
