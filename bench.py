@@ -216,8 +216,10 @@ class Step:
             self.pf_ws = torch.empty(max(256, pa.prefill_workspace_size(1, self.n_chunk_rows, self.max_s)),
                                      dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.launches_per_step = self.layers * ((1 if self.append else 0) + (1 if self.n_chunk_rows else 0)
-                                                + (2 if nd else 0))
+        # kernels per call: append 1; prefill 2 (the chunk kernel and its merge); decode 1 or 2
+        self.dec_kernels = pa.decode_kernels_per_call(nd, self.max_s) if nd else 0
+        self.launches_per_step = self.layers * ((1 if self.append else 0) + (2 if self.n_chunk_rows else 0)
+                                                + self.dec_kernels)
 
     def run(self, events=None, q_src=None, parts=("append", "prefill", "decode")):
         pa, inp = self.pa, self.inp
@@ -502,8 +504,8 @@ def main():
     clocks = sampler.stop(device_uuid()) if rank == 0 else None
     total_s, t_dec, t_pf = max_over_ranks(dist, [total_s, t_dec, t_pf], dev)
     n = world
-    launches = K_ * (step.launches_per_step + (2 * step.layers if g_dec is not None else 0)
-                     + (step.layers if g_pf is not None else 0))
+    launches = K_ * (step.launches_per_step + (step.dec_kernels * step.layers if g_dec is not None else 0)
+                     + (2 * step.layers if g_pf is not None else 0))
     dec_gbs = weak_scaling_rate(step.dec_bytes * step.layers * K_, n, t_dec) / 1e9 if t_dec else None
     pf_tflops = weak_scaling_rate(step.pf_flops * step.layers * K_, n, t_pf) / 1e12 if t_pf else None
 
@@ -538,12 +540,15 @@ def main():
     if t_dec:
         per_launch_s = t_dec / (step.layers * K_)
         ach = step.dec_bytes / per_launch_s / 1e9
-        roofs.append((t_dec, {"kernel": "attn_decode_paged (decode_splitkv + merge)", "bound": "hbm",
+        split = step.dec_kernels == 2   # else the single-launch short-batch path
+        roofs.append((t_dec, {"kernel": "attn_decode_paged (" + ("decode_splitkv + merge" if split else
+                                                                  "decode_cluster, one launch") + ")",
+                              "bound": "hbm",
                               "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(ach / hbm, 4), "peak_source": f"{peak_src} hbm_gbs (a read+write copy)",
                               "frac_of_nominal_8tbs": round(ach / NOMINAL_HBM_GBS, 4),
                               "traffic": traffic_from_profile("decode_splitkv_decode_b16_l27k.md", dec_src,
-                                                              step.dec_bytes),
+                                                              step.dec_bytes) if split else None,
                               "traffic_source": "ncu dram bytes of decode_b16_l27k per algorithmic byte x "
                                                 "this launch's algorithmic bytes",
                               "algorithmic_bytes_per_launch": step.dec_bytes}))
@@ -698,8 +703,9 @@ def bucket_latencies(pa, dev, dist, warmup, layers=28, seq_len=1000):
     its own pools. Two figures per bucket: microseconds per decode call inside one graph of
     ``layers`` calls (one per layer, as in a decoder step's graph), and microseconds per replay
     of a graph holding a single call (which adds the graph launch itself)."""
-    per_call, single, gbs = {}, {}, {}
+    per_call, single, gbs, kernels = {}, {}, {}, {}
     for B in BUCKETS:
+        kernels[str(B)] = pa.decode_kernels_per_call(B, seq_len)
         seed = W.CONFIG_SEED["decode_b1_l1000"] + B
         inp = W.make_paged(seed, np.full(B, seq_len), np.ones(B, np.int64), layers=layers,
                            device=dev, with_new_kv=False)
@@ -727,7 +733,7 @@ def bucket_latencies(pa, dev, dist, warmup, layers=28, seq_len=1000):
         torch.cuda.empty_cache()
     return {"seq_len": seq_len, "us_per_call_in_layer_graph": per_call,
             "us_per_single_call_graph_replay": single, "kv_read_gbs_in_layer_graph": gbs,
-            "layers_per_graph": layers}
+            "kernels_per_call": kernels, "layers_per_graph": layers}
 
 
 def run_decode_buckets(pa, args, dev, dist, world, rank):
@@ -752,11 +758,12 @@ def run_decode_buckets(pa, args, dev, dist, world, rank):
                        "timing": "CUDA events around back-to-back replays of a 28-call graph (one call per "
                                  "layer) and of a one-call graph, per bucket"},
             "buckets": res,
-            "roofline": {"kernel": "attn_decode_paged (decode_splitkv + merge)", "bound": "hbm",
-                         "achieved": g32, "peak": hbm, "unit": "GB/s",
+            "roofline": {"kernel": "attn_decode_paged (decode_splitkv + merge at 32 sequences)",
+                         "bound": "hbm", "achieved": g32, "peak": hbm, "unit": "GB/s",
                          "frac": round(g32 / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
                          "traffic": None, "note": "at the 32-sequence bucket; small buckets are latency-bound"},
-            "gpu_launches": 2 * 200 * (28 + 10) * len(BUCKETS), "clocks": clocks}), flush=True)
+            "gpu_launches": 200 * (28 + 10) * sum(res["kernels_per_call"].values()),
+            "clocks": clocks}), flush=True)
 
 
 def run_reference(args, world, rank):

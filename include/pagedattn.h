@@ -119,16 +119,25 @@ pa_status kv_append_paged(pa_dims dims, const void* k_new, const void* v_new, in
  *                most 64 ranges per SM; any value >= the batch's total keys gives one range.
  *                Negative: PA_ERR_INVALID_ARG. The result does not depend on it beyond
  *                rounding (the split-KV partials are merged exactly by log-sum-exp).
- *   out          bf16 [batch][Hq][128];  lse fp32 [batch][Hq] or NULL
  *   workspace    device scratch of at least pa_decode_workspace_size(dims, batch, max_seq_len,
  *                split_tokens) bytes, 256-byte aligned; holds per-split partial results. With
  *                split_tokens = 0 the size does not depend on max_seq_len. Calls that share a
  *                workspace must not overlap on the GPU.
  * The key range of all sequences is laid end to end and cut into page ranges (split-KV);
- * partial (o, lse) pairs of sequences that span ranges are merged by log-sum-exp.
+ * partial (o, lse) pairs of sequences that span ranges are merged by log-sum-exp (two
+ * kernels). With split_tokens = 0 a short batch (every (sequence, KV head) pair can have a
+ * resident cluster of up to 8 CTAs, each holding at most 64 pages) is served by one kernel
+ * instead: each pair's cluster splits its pages and merges in distributed shared memory; the
+ * workspace is then not touched.
  * ------------------------------------------------------------------------------------------ */
 size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len,
                                 int32_t split_tokens);
+
+/* Kernels one attn_decode_paged call with these arguments launches on the current device: 1
+ * (single-launch short-batch path) or 2 (split kernel + merge); 0 for unsupported dims or
+ * batch <= 0. For sizing CUDA graphs and counting launches; computes nothing on the GPU. */
+int32_t pa_decode_kernels_per_call(pa_dims dims, int32_t batch, int32_t max_seq_len,
+                                   int32_t split_tokens);
 
 pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool, const void* v_pool,
                             int64_t num_pages, const int32_t* block_table, int32_t bt_stride,

@@ -22,7 +22,8 @@ __all__ = [
     "load", "PagedAttnError", "Dims", "DEFAULT_DIMS",
     "kv_append_paged", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_prefill_chunk",
     "attn_merge_lse", "adaptor_mlp_merge4", "adaptor_workspace_size",
-    "decode_workspace_size", "prefill_workspace_size", "read_device_status", "debug_decode_starve",
+    "decode_workspace_size", "decode_kernels_per_call", "prefill_workspace_size",
+    "read_device_status", "debug_decode_starve",
     "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "DEV_ERR_INTERNAL", "lib_path",
 ]
 
@@ -65,6 +66,7 @@ _F = ctypes.c_float
 _SIGS = {
     "kv_append_paged": (_I32, [Dims, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _I64, _P, _P]),
     "pa_decode_workspace_size": (_SZ, [Dims, _I32, _I32, _I32]),
+    "pa_decode_kernels_per_call": (_I32, [Dims, _I32, _I32, _I32]),
     "attn_decode_paged": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _I32, _P, _P,
                                  _P, _SZ, _P, _P]),
     "pa_debug_decode_starve": (_I32, [_I32]),
@@ -212,6 +214,12 @@ def kv_append_paged(k_new, v_new, cu_new_lens, start_pos, block_table, k_pool, v
 
 def decode_workspace_size(batch: int, max_seq_len: int, split_tokens: int = 0, dims=None) -> int:
     return int(load().pa_decode_workspace_size(_dims(dims), batch, max_seq_len, split_tokens))
+
+
+def decode_kernels_per_call(batch: int, max_seq_len: int, split_tokens: int = 0, dims=None) -> int:
+    """Kernels one attn_decode_paged call launches (1: single-launch short-batch path, 2: split
+    kernel + merge; 0 for an empty or unsupported call)."""
+    return int(load().pa_decode_kernels_per_call(_dims(dims), batch, max_seq_len, split_tokens))
 
 
 def prefill_workspace_size(batch: int, max_q_len: int, max_seq_len: int, dims=None) -> int:

@@ -573,6 +573,329 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
   if (lane == 0 && p.lse != nullptr) p.lse[b * hq + h] = (M + log2f(wsum)) * kLn2;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Short batches in one launch (decode_cluster_kernel). When every (sequence, KV head) pair of
+// the batch can have a cluster of C CTAs (C a power of two <= 8, batch x Hkv x C <= SMs) and
+// each CTA then holds few pages, the split above is latency-bound: a prefix pass, a dependent
+// block-table load, one page per SM, partials through L2 and a second kernel that waits for the
+// first to complete. Here CTA rank c of the cluster of pair (b, g) takes pages
+// [cP/C, (c+1)P/C) of sequence b (P = its pages) for KV head g only; its 8 warps take one page
+// each in turn and load their page's K/V rows of head g straight into registers (the next
+// page's rows in flight while the current one is computed); the warps combine through shared
+// memory, the ranks write their partial (o, max, sum) into rank 0's shared memory (distributed
+// shared memory of the cluster) and rank 0 merges them and writes the output.
+// ---------------------------------------------------------------------------------------------
+constexpr int kSmallWarps = 8;
+constexpr int kSmallThreads = kSmallWarps * 32;
+constexpr int kSmallMaxCluster = 8;
+constexpr int kSmallPreload = 256;  // block-table entries loaded beside the length (Pmax <= this)
+constexpr int kSmallMaxPagesPerCta = 64;  // beyond this the full-grid split streams faster
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster (the barrier inits are visible after it)
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// arrive on an mbarrier of another CTA of the cluster, ordering this thread's earlier writes
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+// bounded wait that also acquires writes made by other CTAs of the cluster
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          uint64_t limit_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (i == 0) t0 = global_timer_ns();
+    else if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+struct SmallSmem {
+  int32_t pages[kSmallPreload];              // the sequence's block-table entries (preloaded)
+  float p[kSmallWarps][32];                  // probabilities handed to the V lanes
+  float red_o[kSmallWarps][2][kHeadDim];     // per warp: unnormalised o of both heads
+  float red_m[kSmallWarps][2], red_l[kSmallWarps][2];
+  float slot_o[kSmallMaxCluster][2][kHeadDim];  // rank 0: each rank's partial
+  float slot_m[kSmallMaxCluster][2], slot_l[kSmallMaxCluster][2];
+  uint64_t full;                             // rank 0: the other ranks' partials have landed
+};
+
+template <int kHkvT>
+__global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const DecodeParams p) {
+  constexpr int kHqT = kGroup * kHkvT;
+  constexpr int64_t kPageBytes = kPage * kHkvT * kHeadDim * 2;  // K (or V) of one page
+  constexpr int kTokenBytes = kHkvT * kHeadDim * 2;             // one token's row in a page
+  __shared__ __align__(16) SmallSmem s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
+  const int pair = static_cast<int>(blockIdx.x / C);  // (sequence, KV head)
+  const int b = pair / kHkvT, g = pair % kHkvT;
+  if (rank == 0 && tid == 0) {
+    mbar_init(&s.full, (C - 1) * kSmallThreads);
+    fence_mbar_init();
+  }
+  cluster_sync_all();  // rank 0's barrier is initialised before any rank can arrive on it
+  // a programmatic dependent of the previous kernel on the stream: nothing it wrote is read
+  // before this wait; the next kernel may launch now and waits for this grid's completion
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+  const int pmax = min((p.max_seq_len + kPage - 1) / kPage, p.bt_stride);
+  const bool preload = pmax <= kSmallPreload;
+  if (preload)
+    for (int i = tid; i < pmax; i += kSmallThreads) s.pages[i] = bt_row[i];
+  const int L = clamp_len(p, b, rank == 0 && g == 0 && tid == 0);
+  const int P = (L + kPage - 1) / kPage;
+  const int p0 = static_cast<int>(static_cast<int64_t>(rank) * P / C);
+  const int p1 = static_cast<int>(static_cast<int64_t>(rank + 1) * P / C);
+
+  // ---- this lane's share of the group's two query rows (dims 8c .. 8c+7), in log2 units
+  const int c = lane & 15, th = lane >> 4;
+  const bool hi_head = (c & 8) != 0;
+  float2 qa[4], qb[4];
+  {
+    const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHqT + 2 * g) * kHeadDim + 8 * c;
+    const uint4 ra = *reinterpret_cast<const uint4*>(qrow);
+    const uint4 rb = *reinterpret_cast<const uint4*>(qrow + kHeadDim);
+    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qa[i] = make_float2(bf16lo(wa[i]) * p.scale_log2, bf16hi(wa[i]) * p.scale_log2);
+      qb[i] = make_float2(bf16lo(wb[i]) * p.scale_log2, bf16hi(wb[i]) * p.scale_log2);
+    }
+  }
+  __syncthreads();  // the preloaded block-table entries
+
+  // the K and V rows of head g this lane reads from page `entry`: tokens th*8 .. th*8+7
+  const int64_t lane_off = static_cast<int64_t>(th * 8) * kTokenBytes + g * (kHeadDim * 2) + c * 16;
+  auto page_entry = [&](int lp) {
+    int e = preload ? s.pages[lp] : bt_row[lp];
+    if (e < 0 || e >= p.num_pages) {
+      flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
+      e = 0;
+    }
+    return e;
+  };
+  auto load_page = [&](int e, uint4 (&kr)[8], uint4 (&vr)[8]) {
+    const uint8_t* kp = p.k_pool + static_cast<int64_t>(e) * kPageBytes + lane_off;
+    const uint8_t* vp = p.v_pool + static_cast<int64_t>(e) * kPageBytes + lane_off;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) kr[j] = *reinterpret_cast<const uint4*>(kp + j * kTokenBytes);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) vr[j] = *reinterpret_cast<const uint4*>(vp + j * kTokenBytes);
+  };
+
+  float2 acc_a[4], acc_b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc_a[i] = acc_b[i] = make_float2(0.f, 0.f);
+  float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F;  // max used for the exponent, per head
+  float l_part = 0.f;                               // this lane's share of its head's sum
+  uint4 kr[8], vr[8];
+  int lp = p0 + warp;
+  if (lp < p1) load_page(page_entry(lp), kr, vr);
+  for (; lp < p1; lp += kSmallWarps) {
+    const int n_valid = min(kPage, L - lp * kPage);
+    uint4 nk[8], nv[8];
+    const bool next = lp + kSmallWarps < p1;
+    if (next) load_page(page_entry(lp + kSmallWarps), nk, nv);
+    // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 k0 = make_float2(bf16lo(kr[j].x), bf16hi(kr[j].x));
+      const float2 k1 = make_float2(bf16lo(kr[j].y), bf16hi(kr[j].y));
+      const float2 k2 = make_float2(bf16lo(kr[j].z), bf16hi(kr[j].z));
+      const float2 k3 = make_float2(bf16lo(kr[j].w), bf16hi(kr[j].w));
+      float2 sa = mul2(qa[0], k0), sb = mul2(qb[0], k0);
+      sa = fma2(qa[1], k1, sa); sb = fma2(qb[1], k1, sb);
+      sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
+      sa = fma2(qa[3], k3, sa); sb = fma2(qb[3], k3, sb);
+      v[j] = sa.x + sa.y;
+      v[8 + j] = sb.x + sb.y;
+    }
+    // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score of
+    //      token th*8 + (c & 7), head (c >> 3)
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+      const bool up = (c & w) != 0;
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const float send = up ? v[i] : v[w + i];
+        const float keep = up ? v[w + i] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+      }
+    }
+    const float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
+    // ---- page max per head, lazily moved running max (at least one key of a page is valid)
+    float pm = sc;
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+    const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
+    const float pmax_a = hi_head ? pm_other : pm;
+    const float pmax_b = hi_head ? pm : pm_other;
+    if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
+      const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
+      const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
+      const float al_b = (m_b == -CUDART_INF_F) ? 0.f : fast_exp2(m_b - nb);
+      const float2 fa = make_float2(al_a, al_a), fb = make_float2(al_b, al_b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc_a[i] = mul2(acc_a[i], fa);
+        acc_b[i] = mul2(acc_b[i], fb);
+      }
+      l_part *= hi_head ? al_b : al_a;
+      m_a = na;
+      m_b = nb;
+    }
+    const float pr = fast_exp2(sc - (hi_head ? m_b : m_a));
+    l_part += pr;
+    // ---- hand probabilities to the lanes that own the V dims
+    s.p[warp][lane] = pr;
+    __syncwarp();
+    const float4 pa0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 0]);
+    const float4 pa1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 4]);
+    const float4 pb0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 8]);
+    const float4 pb1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 12]);
+    __syncwarp();  // read before the next page overwrites them
+    const float pav[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
+    const float pbv[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
+    // ---- o += p v over this lane's 8 tokens (invalid slots of a partial page skipped)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (th * 8 + j < n_valid) {
+        const float2 ppa = make_float2(pav[j], pav[j]);
+        const float2 ppb = make_float2(pbv[j], pbv[j]);
+        const float2 v0 = make_float2(bf16lo(vr[j].x), bf16hi(vr[j].x));
+        const float2 v1 = make_float2(bf16lo(vr[j].y), bf16hi(vr[j].y));
+        const float2 v2 = make_float2(bf16lo(vr[j].z), bf16hi(vr[j].z));
+        const float2 v3 = make_float2(bf16lo(vr[j].w), bf16hi(vr[j].w));
+        acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
+        acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
+        acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
+        acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
+      }
+    }
+    if (next) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        kr[j] = nk[j];
+        vr[j] = nv[j];
+      }
+    }
+  }
+
+  // ---- this warp's (m, sum, unnormalised o) per head: lanes 0..15 head 2g, 16..31 head 2g+1
+  float l_m = l_part;
+  l_m += __shfl_xor_sync(0xffffffffu, l_m, 1);
+  l_m += __shfl_xor_sync(0xffffffffu, l_m, 2);
+  l_m += __shfl_xor_sync(0xffffffffu, l_m, 4);
+  l_m += __shfl_xor_sync(0xffffffffu, l_m, 16);
+  const float l_o = __shfl_xor_sync(0xffffffffu, l_m, 8);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc_a[i].x += __shfl_xor_sync(0xffffffffu, acc_a[i].x, 16);
+    acc_a[i].y += __shfl_xor_sync(0xffffffffu, acc_a[i].y, 16);
+    acc_b[i].x += __shfl_xor_sync(0xffffffffu, acc_b[i].x, 16);
+    acc_b[i].y += __shfl_xor_sync(0xffffffffu, acc_b[i].y, 16);
+  }
+  {
+    float* dst = &s.red_o[warp][th][8 * c];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = th ? acc_b[i] : acc_a[i];
+      dst[2 * i] = a.x;
+      dst[2 * i + 1] = a.y;
+    }
+    if (c == 0) {
+      s.red_m[warp][th] = th ? m_b : m_a;
+      s.red_l[warp][th] = th ? (hi_head ? l_m : l_o) : (hi_head ? l_o : l_m);
+    }
+  }
+  __syncthreads();
+
+  // ---- this CTA's partial per head: thread (h2, d) combines the 8 warps for dim d of head 2g+h2
+  const int h2 = tid >> 7, d = tid & (kHeadDim - 1);
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int w = 0; w < kSmallWarps; ++w) M = fmaxf(M, s.red_m[w][h2]);
+  float o = 0.f, l = 0.f;
+  {
+    const float Ms = M == -CUDART_INF_F ? 0.f : M;  // a warp without pages weighs 0
+#pragma unroll
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const float sw = fast_exp2(s.red_m[w][h2] - Ms);
+      o += sw * s.red_o[w][h2][d];
+      l += sw * s.red_l[w][h2];
+    }
+  }
+  if (C > 1) {
+    if (rank != 0) {
+      // into rank 0's slot for this rank, then one arrive per thread on rank 0's barrier
+      st_cluster_f32(map_to_rank(&s.slot_o[rank][h2][d], 0), o);
+      if (d == 0) {
+        st_cluster_f32(map_to_rank(&s.slot_m[rank][h2], 0), M);
+        st_cluster_f32(map_to_rank(&s.slot_l[rank][h2], 0), l);
+      }
+      mbar_arrive_cluster(map_to_rank(&s.full, 0));
+      return;
+    }
+    if (!mbar_wait_cluster_bounded(&s.full, 0, p.wait_limit_ns)) {
+      flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+      return;
+    }
+    float Mc = M;
+    for (uint32_t r = 1; r < C; ++r) Mc = fmaxf(Mc, s.slot_m[r][h2]);
+    const float Ms = Mc == -CUDART_INF_F ? 0.f : Mc;
+    const float s0 = fast_exp2(M - Ms);
+    o *= s0;
+    l *= s0;
+    for (uint32_t r = 1; r < C; ++r) {
+      const float sr = fast_exp2(s.slot_m[r][h2] - Ms);
+      o += sr * s.slot_o[r][h2][d];
+      l += sr * s.slot_l[r][h2];
+    }
+    M = Mc;
+  }
+  // an empty sequence has l = 0, M = -inf: o = 0 and lse = -inf
+  const int head = 2 * g + h2;
+  const float inv = l > 0.f ? 1.0f / l : 0.f;
+  p.out[(static_cast<int64_t>(b) * kHqT + head) * kHeadDim + d] =
+      static_cast<uint16_t>(pack_bf16x2(o * inv, 0.f) & 0xffffu);
+  if (d == 0 && p.lse != nullptr) p.lse[b * kHqT + head] = (M + log2f(l)) * kLn2;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
@@ -629,9 +952,60 @@ DecodePlan decode_plan(int batch, int max_seq_len, int split_tokens, int sm_grid
   return d;
 }
 
+// Clusters of decode_cluster_kernel of size C (1, 2, 4 or 8) that the current device can hold
+// at once, from the occupancy calculator (0 if it cannot say: the split path then serves the
+// call); cached per device and size.
+int small_cluster_capacity(int C) {
+  static std::mutex mu;
+  static int cache[64][4];
+  static bool known[64][4] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int k = C == 1 ? 0 : (C == 2 ? 1 : (C == 4 ? 2 : 3));
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev][k]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(C * 256));
+    cfg.blockDim = dim3(kSmallThreads);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    // every instance of the kernel has the same registers and shared memory
+    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<8>, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // not sticky: clear it; the split path serves this call, and the
+      return 0;            // query is repeated on the next call
+    }
+    cache[dev][k] = n;
+    known[dev][k] = true;
+  }
+  return cache[dev][k];
+}
+
 // Test hook (pa_debug_decode_starve): the calling thread's next launches leave one ring stage
 // of CTA 0 empty and bound every wait by 1 ms.
 thread_local bool g_debug_starve = false;
+
+// How a call is served: the cluster size C of the single-launch path, or 0 for the split path
+// (split kernel + merge). The single launch is taken with the automatic split when every
+// (sequence, KV head) pair can have a resident cluster of C CTAs (the largest such C <= 8) and
+// a CTA then holds at most kSmallMaxPagesPerCta pages; the bounded-wait test hook keeps the
+// split path, whose ring it exercises.
+int small_path_cluster(int hkv, int batch, int max_seq_len, int split_tokens) {
+  if (split_tokens != 0 || g_debug_starve || batch <= 0) return 0;
+  const int64_t pairs = static_cast<int64_t>(batch) * hkv;
+  const int64_t pmax = (static_cast<int64_t>(max_seq_len) + kPage - 1) / kPage;
+  // the largest cluster size whose clusters can all be resident at once (a cluster must fit in
+  // one GPC, so this can be fewer than SMs / C)
+  int C = kSmallMaxCluster;
+  while (C > 1 && pairs > small_cluster_capacity(C)) C >>= 1;
+  if (pairs <= small_cluster_capacity(C) && (pmax + C - 1) / C <= kSmallMaxPagesPerCta) return C;
+  return 0;
+}
 constexpr uint64_t kDebugWaitLimitNs = 1000000ull;
 
 }  // namespace
@@ -652,6 +1026,13 @@ extern "C" size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t 
 extern "C" pa_status pa_debug_decode_starve(int32_t enable) {
   pa::g_debug_starve = enable != 0;
   return PA_OK;
+}
+
+extern "C" int32_t pa_decode_kernels_per_call(pa_dims dims, int32_t batch, int32_t max_seq_len,
+                                              int32_t split_tokens) {
+  if (!pa::gqa_dims_supported(dims) || batch <= 0 || max_seq_len < 0 || split_tokens < 0)
+    return 0;
+  return pa::small_path_cluster(dims.num_kv_heads, batch, max_seq_len, split_tokens) > 0 ? 1 : 2;
 }
 
 extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool,
@@ -735,6 +1116,35 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   p.starve = g_debug_starve ? 1 : 0;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // Short batches in one launch (decode_cluster_kernel; see small_path_cluster)
+  {
+    const int C = small_path_cluster(hkv, batch, max_seq_len, split_tokens);
+    if (C > 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(batch) * static_cast<unsigned>(hkv * C));
+      cfg.blockDim = dim3(kSmallThreads);
+      cfg.dynamicSmemBytes = 0;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      cudaError_t e;
+      switch (hkv) {
+        case 8: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<8>, p); break;
+        case 4: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<4>, p); break;
+        case 2: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<2>, p); break;
+        default: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<1>, p); break;
+      }
+      if (e != cudaSuccess) return record_cuda_error(e, "decode_cluster_kernel");
+      return PA_OK;
+    }
+  }
   {
     // a programmatic dependent of the previous work on the stream: it may launch during that
     // work's tail and waits (griddepcontrol.wait) before reading any input

@@ -46,15 +46,21 @@ def test_decode_small(cuda_lib, lens):
 
 @pytest.mark.parametrize("lens", [[1000] * 2, [1000] * 4, [1000] * 8, [5000, 20, 7000]])
 def test_decode_few_sequences_many_partials(cuda_lib, lens):
-    """Few sequences spread over many CTAs, so each is cut into tens of partials and merged by
-    16 warps per head; the last case gives the sequences very different partial counts (two
-    rounds of the warp loop for the longest, one partial for the shortest)."""
+    """Few sequences, both ways: with the automatic split they go to the single-launch path (a
+    cluster of CTAs per sequence and KV head, merged in distributed shared memory); with one page
+    per range (split_tokens=16) each is cut into tens of partials merged by 16 warps per head,
+    and the last case gives the sequences very different partial counts (two rounds of the warp
+    loop for the longest, one partial for the shortest)."""
     inp = W.make_paged(91 + len(lens), lens, [1] * len(lens), poison=True, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out, lse = run_decode(cuda_lib, inp, status=status)
     ref_o, ref_l = oracle_decode(inp)
-    check_attn(out, lse, ref_o, ref_l, what=f"decode {lens}")
-    assert cuda_lib.read_device_status(status) == 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for split in (0, 16):
+        out, lse = cuda_lib.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0],
+                                              inp.block_table, inp.seq_lens, max(lens), inp.scale,
+                                              split_tokens=split, status=status)
+        torch.cuda.synchronize()
+        check_attn(out, lse, ref_o, ref_l, what=f"decode {lens}, split_tokens={split}")
+        assert cuda_lib.read_device_status(status) == 0
 
 
 @pytest.mark.parametrize("name,scale_down", [("decode_b16_l27k", 10), ("decode_ragged_b64", 10)])
@@ -180,12 +186,14 @@ def test_decode_workspace_too_small_is_rejected(cuda_lib):
 SPLITS = [0, 16, 256, 1024, 4096, 2**31 - 1]
 
 
-@pytest.mark.parametrize("lens", [[4000, 123, 2049, 0, 16, 30000, 1], [1000] * 4 + [70000]])
+@pytest.mark.parametrize("lens", [[4000, 123, 2049, 0, 16, 30000, 1], [1000] * 4 + [70000],
+                                  [300, 17, 0, 1000, 1, 64]])
 def test_decode_split_count_invariance(cuda_lib, lens):
     """split_tokens in {auto, 16, 256, 1024, 4096, one range}: the key ranges and so the number
     of partials per sequence differ (from one page per range to a single CTA for the whole
     batch); every result matches the oracle, and all agree with each other within the same
-    tolerance (the split sizes are whole pages)."""
+    tolerance (the split sizes are whole pages). With the short lengths of the last case the
+    automatic choice is the single-launch cluster path."""
     pa = cuda_lib
     inp = W.make_paged(17 + len(lens), lens, [1] * len(lens), poison=True, device="cuda")
     ref_o, ref_l = oracle_decode(inp)
