@@ -644,21 +644,27 @@ struct SmallSmem {
   float p[kSmallWarps][32];                  // probabilities handed to the V lanes
   float red_o[kSmallWarps][2][kHeadDim];     // per warp: unnormalised o of both heads
   float red_m[kSmallWarps][2], red_l[kSmallWarps][2];
-  float slot_o[kSmallMaxCluster][2][kHeadDim];  // rank 0: each rank's partial
-  float slot_m[kSmallMaxCluster][2], slot_l[kSmallMaxCluster][2];
+  float slot_o[kSmallMaxCluster][4][kHeadDim];  // rank 0: each rank's partial (query heads)
+  float slot_m[kSmallMaxCluster][4], slot_l[kSmallMaxCluster][4];
   uint64_t full;                             // rank 0: the other ranks' partials have landed
 };
 
-template <int kHkvT>
+// kHpc KV heads per CTA (1, or 2 when a batch has more (sequence, KV head) pairs than the GPU
+// has SMs): warps w / (8 / kHpc) serve the CTA's head w / (8 / kHpc).
+template <int kHkvT, int kHpc>
 __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const DecodeParams p) {
+  static_assert(kHpc == 1 || kHpc == 2, "one or two KV heads per CTA");
   constexpr int kHqT = kGroup * kHkvT;
+  constexpr int kWph = kSmallWarps / kHpc;  // warps per KV head
   constexpr int64_t kPageBytes = kPage * kHkvT * kHeadDim * 2;  // K (or V) of one page
   constexpr int kTokenBytes = kHkvT * kHeadDim * 2;             // one token's row in a page
   __shared__ __align__(16) SmallSmem s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
-  const int pair = static_cast<int>(blockIdx.x / C);  // (sequence, KV head)
-  const int b = pair / kHkvT, g = pair % kHkvT;
+  const int pair = static_cast<int>(blockIdx.x / C);  // (sequence, group of kHpc KV heads)
+  const int b = pair / (kHkvT / kHpc);
+  const int g0 = (pair % (kHkvT / kHpc)) * kHpc;      // the CTA's first KV head
+  const int hh = warp / kWph, g = g0 + hh;            // this warp's KV head
   if (rank == 0 && tid == 0) {
     mbar_init(&s.full, (C - 1) * kSmallThreads);
     fence_mbar_init();
@@ -674,7 +680,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
   const bool preload = pmax <= kSmallPreload;
   if (preload)
     for (int i = tid; i < pmax; i += kSmallThreads) s.pages[i] = bt_row[i];
-  const int L = clamp_len(p, b, rank == 0 && g == 0 && tid == 0);
+  const int L = clamp_len(p, b, rank == 0 && g0 == 0 && tid == 0);
   const int P = (L + kPage - 1) / kPage;
   const int p0 = static_cast<int>(static_cast<int64_t>(rank) * P / C);
   const int p1 = static_cast<int>(static_cast<int64_t>(rank + 1) * P / C);
@@ -721,13 +727,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
   float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F;  // max used for the exponent, per head
   float l_part = 0.f;                               // this lane's share of its head's sum
   uint4 kr[8], vr[8];
-  int lp = p0 + warp;
+  int lp = p0 + warp % kWph;
   if (lp < p1) load_page(page_entry(lp), kr, vr);
-  for (; lp < p1; lp += kSmallWarps) {
+  for (; lp < p1; lp += kWph) {
     const int n_valid = min(kPage, L - lp * kPage);
     uint4 nk[8], nv[8];
-    const bool next = lp + kSmallWarps < p1;
-    if (next) load_page(page_entry(lp + kSmallWarps), nk, nv);
+    const bool next = lp + kWph < p1;
+    if (next) load_page(page_entry(lp + kWph), nk, nv);
     // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
     float v[16];
 #pragma unroll
@@ -845,28 +851,40 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
   }
   __syncthreads();
 
-  // ---- this CTA's partial per head: thread (h2, d) combines the 8 warps for dim d of head 2g+h2
-  const int h2 = tid >> 7, d = tid & (kHeadDim - 1);
-  float M = -CUDART_INF_F;
+  // ---- this CTA's partial per query head: thread tid + 256k takes dim d of the CTA's query head
+  //      qh = 2 hh + h2 (head 2 g0 + qh), combining the warps that served KV head g0 + hh
+  float o[kHpc], l[kHpc], M[kHpc];
 #pragma unroll
-  for (int w = 0; w < kSmallWarps; ++w) M = fmaxf(M, s.red_m[w][h2]);
-  float o = 0.f, l = 0.f;
-  {
-    const float Ms = M == -CUDART_INF_F ? 0.f : M;  // a warp without pages weighs 0
+  for (int k = 0; k < kHpc; ++k) {
+    const int qh = (tid + k * kSmallThreads) >> 7, d = tid & (kHeadDim - 1);
+    const int wh = qh >> 1, h2 = qh & 1;
+    float m = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < kSmallWarps; ++w) {
-      const float sw = fast_exp2(s.red_m[w][h2] - Ms);
-      o += sw * s.red_o[w][h2][d];
-      l += sw * s.red_l[w][h2];
+    for (int w = 0; w < kWph; ++w) m = fmaxf(m, s.red_m[wh * kWph + w][h2]);
+    const float ms = m == -CUDART_INF_F ? 0.f : m;  // a warp without pages weighs 0
+    float oo = 0.f, ll = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWph; ++w) {
+      const int ww = wh * kWph + w;
+      const float sw = fast_exp2(s.red_m[ww][h2] - ms);
+      oo += sw * s.red_o[ww][h2][d];
+      ll += sw * s.red_l[ww][h2];
     }
+    o[k] = oo;
+    l[k] = ll;
+    M[k] = m;
   }
   if (C > 1) {
     if (rank != 0) {
       // into rank 0's slot for this rank, then one arrive per thread on rank 0's barrier
-      st_cluster_f32(map_to_rank(&s.slot_o[rank][h2][d], 0), o);
-      if (d == 0) {
-        st_cluster_f32(map_to_rank(&s.slot_m[rank][h2], 0), M);
-        st_cluster_f32(map_to_rank(&s.slot_l[rank][h2], 0), l);
+#pragma unroll
+      for (int k = 0; k < kHpc; ++k) {
+        const int qh = (tid + k * kSmallThreads) >> 7, d = tid & (kHeadDim - 1);
+        st_cluster_f32(map_to_rank(&s.slot_o[rank][qh][d], 0), o[k]);
+        if (d == 0) {
+          st_cluster_f32(map_to_rank(&s.slot_m[rank][qh], 0), M[k]);
+          st_cluster_f32(map_to_rank(&s.slot_l[rank][qh], 0), l[k]);
+        }
       }
       mbar_arrive_cluster(map_to_rank(&s.full, 0));
       return;
@@ -875,25 +893,34 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
       flag_error(p.status, PA_DEV_ERR_TIMEOUT);
       return;
     }
-    float Mc = M;
-    for (uint32_t r = 1; r < C; ++r) Mc = fmaxf(Mc, s.slot_m[r][h2]);
-    const float Ms = Mc == -CUDART_INF_F ? 0.f : Mc;
-    const float s0 = fast_exp2(M - Ms);
-    o *= s0;
-    l *= s0;
-    for (uint32_t r = 1; r < C; ++r) {
-      const float sr = fast_exp2(s.slot_m[r][h2] - Ms);
-      o += sr * s.slot_o[r][h2][d];
-      l += sr * s.slot_l[r][h2];
+#pragma unroll
+    for (int k = 0; k < kHpc; ++k) {
+      const int qh = (tid + k * kSmallThreads) >> 7, d = tid & (kHeadDim - 1);
+      float mc = M[k];
+      for (uint32_t r = 1; r < C; ++r) mc = fmaxf(mc, s.slot_m[r][qh]);
+      const float ms = mc == -CUDART_INF_F ? 0.f : mc;
+      const float s0 = fast_exp2(M[k] - ms);
+      float oo = o[k] * s0, ll = l[k] * s0;
+      for (uint32_t r = 1; r < C; ++r) {
+        const float sr = fast_exp2(s.slot_m[r][qh] - ms);
+        oo += sr * s.slot_o[r][qh][d];
+        ll += sr * s.slot_l[r][qh];
+      }
+      o[k] = oo;
+      l[k] = ll;
+      M[k] = mc;
     }
-    M = Mc;
   }
   // an empty sequence has l = 0, M = -inf: o = 0 and lse = -inf
-  const int head = 2 * g + h2;
-  const float inv = l > 0.f ? 1.0f / l : 0.f;
-  p.out[(static_cast<int64_t>(b) * kHqT + head) * kHeadDim + d] =
-      static_cast<uint16_t>(pack_bf16x2(o * inv, 0.f) & 0xffffu);
-  if (d == 0 && p.lse != nullptr) p.lse[b * kHqT + head] = (M + log2f(l)) * kLn2;
+#pragma unroll
+  for (int k = 0; k < kHpc; ++k) {
+    const int qh = (tid + k * kSmallThreads) >> 7, d = tid & (kHeadDim - 1);
+    const int head = 2 * g0 + qh;
+    const float inv = l[k] > 0.f ? 1.0f / l[k] : 0.f;
+    p.out[(static_cast<int64_t>(b) * kHqT + head) * kHeadDim + d] =
+        static_cast<uint16_t>(pack_bf16x2(o[k] * inv, 0.f) & 0xffffu);
+    if (d == 0 && p.lse != nullptr) p.lse[b * kHqT + head] = (M[k] + log2f(l[k])) * kLn2;
+  }
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -955,15 +982,15 @@ DecodePlan decode_plan(int batch, int max_seq_len, int split_tokens, int sm_grid
 // Clusters of decode_cluster_kernel of size C (1, 2, 4 or 8) that the current device can hold
 // at once, from the occupancy calculator (0 if it cannot say: the split path then serves the
 // call); cached per device and size.
-int small_cluster_capacity(int C) {
+int small_cluster_capacity(int C, int hpc) {
   static std::mutex mu;
-  static int cache[64][4];
-  static bool known[64][4] = {};
+  static int cache[64][2][4];
+  static bool known[64][2][4] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int k = C == 1 ? 0 : (C == 2 ? 1 : (C == 4 ? 2 : 3));
+  const int k = C == 1 ? 0 : (C == 2 ? 1 : (C == 4 ? 2 : 3)), h = hpc == 2 ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (!known[dev][k]) {
+  if (!known[dev][h][k]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(C * 256));
     cfg.blockDim = dim3(kSmallThreads);
@@ -975,36 +1002,50 @@ int small_cluster_capacity(int C) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    // every instance of the kernel has the same registers and shared memory
-    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<8>, &cfg) != cudaSuccess) {
+    // the instances for other KV-head counts use the same registers and shared memory
+    const cudaError_t e = hpc == 2
+        ? cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<8, 2>, &cfg)
+        : cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<8, 1>, &cfg);
+    if (e != cudaSuccess) {
       cudaGetLastError();  // not sticky: clear it; the split path serves this call, and the
       return 0;            // query is repeated on the next call
     }
-    cache[dev][k] = n;
-    known[dev][k] = true;
+    cache[dev][h][k] = n;
+    known[dev][h][k] = true;
   }
-  return cache[dev][k];
+  return cache[dev][h][k];
 }
 
 // Test hook (pa_debug_decode_starve): the calling thread's next launches leave one ring stage
 // of CTA 0 empty and bound every wait by 1 ms.
 thread_local bool g_debug_starve = false;
 
-// How a call is served: the cluster size C of the single-launch path, or 0 for the split path
-// (split kernel + merge). The single launch is taken with the automatic split when every
-// (sequence, KV head) pair can have a resident cluster of C CTAs (the largest such C <= 8) and
-// a CTA then holds at most kSmallMaxPagesPerCta pages; the bounded-wait test hook keeps the
-// split path, whose ring it exercises.
-int small_path_cluster(int hkv, int batch, int max_seq_len, int split_tokens) {
-  if (split_tokens != 0 || g_debug_starve || batch <= 0) return 0;
-  const int64_t pairs = static_cast<int64_t>(batch) * hkv;
+// How a call is served: the single-launch path with clusters of C CTAs of hpc KV heads each, or
+// (C = 0) the split path (split kernel + merge). The single launch is taken with the automatic
+// split when every (sequence, group of hpc KV heads) can have a resident cluster of C CTAs (the
+// largest such C <= 8; one head per CTA first, two if the batch has more pairs than that) and a
+// CTA then holds at most kSmallMaxPagesPerCta pages; the bounded-wait test hook keeps the split
+// path, whose ring it exercises.
+struct SmallPath {
+  int C = 0, hpc = 0;
+};
+SmallPath small_path(int hkv, int batch, int max_seq_len, int split_tokens) {
+  SmallPath r;
+  if (split_tokens != 0 || g_debug_starve || batch <= 0) return r;
   const int64_t pmax = (static_cast<int64_t>(max_seq_len) + kPage - 1) / kPage;
-  // the largest cluster size whose clusters can all be resident at once (a cluster must fit in
-  // one GPC, so this can be fewer than SMs / C)
-  int C = kSmallMaxCluster;
-  while (C > 1 && pairs > small_cluster_capacity(C)) C >>= 1;
-  if (pairs <= small_cluster_capacity(C) && (pmax + C - 1) / C <= kSmallMaxPagesPerCta) return C;
-  return 0;
+  for (int hpc = 1; hpc <= 2 && hkv % hpc == 0; hpc *= 2) {
+    const int64_t pairs = static_cast<int64_t>(batch) * (hkv / hpc);
+    // the largest cluster size whose clusters can all be resident at once (a cluster must fit
+    // in one GPC, so this can be fewer than SMs / C)
+    int C = kSmallMaxCluster;
+    while (C > 1 && pairs > small_cluster_capacity(C, hpc)) C >>= 1;
+    if (pairs <= small_cluster_capacity(C, hpc) && (pmax + C - 1) / C <= kSmallMaxPagesPerCta) {
+      r.C = C;
+      r.hpc = hpc;
+      return r;
+    }
+  }
+  return r;
 }
 constexpr uint64_t kDebugWaitLimitNs = 1000000ull;
 
@@ -1032,7 +1073,7 @@ extern "C" int32_t pa_decode_kernels_per_call(pa_dims dims, int32_t batch, int32
                                               int32_t split_tokens) {
   if (!pa::gqa_dims_supported(dims) || batch <= 0 || max_seq_len < 0 || split_tokens < 0)
     return 0;
-  return pa::small_path_cluster(dims.num_kv_heads, batch, max_seq_len, split_tokens) > 0 ? 1 : 2;
+  return pa::small_path(dims.num_kv_heads, batch, max_seq_len, split_tokens).C > 0 ? 1 : 2;
 }
 
 extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool,
@@ -1116,12 +1157,13 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   p.starve = g_debug_starve ? 1 : 0;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // Short batches in one launch (decode_cluster_kernel; see small_path_cluster)
+  // Short batches in one launch (decode_cluster_kernel; see small_path)
   {
-    const int C = small_path_cluster(hkv, batch, max_seq_len, split_tokens);
-    if (C > 0) {
+    const SmallPath sp = small_path(hkv, batch, max_seq_len, split_tokens);
+    if (sp.C > 0) {
+      const int C = sp.C;
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(batch) * static_cast<unsigned>(hkv * C));
+      cfg.gridDim = dim3(static_cast<unsigned>(batch) * static_cast<unsigned>(hkv / sp.hpc * C));
       cfg.blockDim = dim3(kSmallThreads);
       cfg.dynamicSmemBytes = 0;
       cfg.stream = st;
@@ -1135,11 +1177,15 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
       cfg.attrs = attr;
       cfg.numAttrs = 2;
       cudaError_t e;
+      const bool two = sp.hpc == 2;
       switch (hkv) {
-        case 8: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<8>, p); break;
-        case 4: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<4>, p); break;
-        case 2: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<2>, p); break;
-        default: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<1>, p); break;
+        case 8: e = two ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<8, 2>, p)
+                        : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<8, 1>, p); break;
+        case 4: e = two ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<4, 2>, p)
+                        : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<4, 1>, p); break;
+        case 2: e = two ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<2, 2>, p)
+                        : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<2, 1>, p); break;
+        default: e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<1, 1>, p); break;
       }
       if (e != cudaSuccess) return record_cuda_error(e, "decode_cluster_kernel");
       return PA_OK;

@@ -34,6 +34,7 @@ def oracle_decode(inp, layer=0, seqs=None):
     [0, 5, 0, 300, 0],
     [0],
     list(range(1, 40)),
+    [17, 300, 0, 1000, 999, 64] * 4,   # 24 sequences: two KV heads per CTA on the single launch
 ])
 def test_decode_small(cuda_lib, lens):
     inp = W.make_paged(77 + len(lens), lens, [1] * len(lens), poison=True, device="cuda")
