@@ -580,10 +580,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
 // block-table load, one page per SM, partials through L2 and a second kernel that waits for the
 // first to complete. Here CTA rank c of the cluster of pair (b, g) takes pages
 // [cP/C, (c+1)P/C) of sequence b (P = its pages) for KV head g only; its 8 warps take one page
-// each in turn and load their page's K/V rows of head g straight into registers (the next
-// page's rows in flight while the current one is computed); the warps combine through shared
-// memory, the ranks write their partial (o, max, sum) into rank 0's shared memory (distributed
-// shared memory of the cluster) and rank 0 merges them and writes the output.
+// each in turn, each warp streaming its pages' K/V rows of head g into its own 3-stage ring
+// (one 256-byte bulk copy per lane and row, two pages in flight ahead of the one computed); the
+// warps combine through shared memory, the ranks write their partial (o, max, sum) into rank 0's
+// shared memory (distributed shared memory of the cluster) and rank 0 merges them and writes
+// the output.
 // ---------------------------------------------------------------------------------------------
 constexpr int kSmallWarps = 8;
 constexpr int kSmallThreads = kSmallWarps * 32;
@@ -639,7 +640,12 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
   }
 }
 
-struct SmallSmem {
+constexpr int kRingStages = 3;                  // pages in flight per warp (incl. the current)
+constexpr int kRowBytes = kHeadDim * 2;         // one token's row of one head
+constexpr int kSlice = kPage * kRowBytes;       // one page of one head: K (or V) rows
+
+struct SmallSmem {  // dynamic shared memory, 128-byte aligned
+  uint8_t ring[kSmallWarps][kRingStages][2][kSlice];  // per warp: its lanes' K and V pieces
   int32_t pages[kSmallPreload];              // the sequence's block-table entries (preloaded)
   float p[kSmallWarps][32];                  // probabilities handed to the V lanes
   float red_o[kSmallWarps][2][kHeadDim];     // per warp: unnormalised o of both heads
@@ -658,15 +664,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
   constexpr int kWph = kSmallWarps / kHpc;  // warps per KV head
   constexpr int64_t kPageBytes = kPage * kHkvT * kHeadDim * 2;  // K (or V) of one page
   constexpr int kTokenBytes = kHkvT * kHeadDim * 2;             // one token's row in a page
-  __shared__ __align__(16) SmallSmem s;
+  extern __shared__ __align__(128) uint8_t small_smem_raw[];
+  SmallSmem& s = *reinterpret_cast<SmallSmem*>(small_smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
   const int pair = static_cast<int>(blockIdx.x / C);  // (sequence, group of kHpc KV heads)
   const int b = pair / (kHkvT / kHpc);
   const int g0 = (pair % (kHkvT / kHpc)) * kHpc;      // the CTA's first KV head
   const int hh = warp / kWph, g = g0 + hh;            // this warp's KV head
-  if (rank == 0 && tid == 0) {
-    mbar_init(&s.full, (C - 1) * kSmallThreads);
+  if (tid == 0) {
+    if (rank == 0) mbar_init(&s.full, (C - 1) * kSmallThreads);
     fence_mbar_init();
   }
   cluster_sync_all();  // rank 0's barrier is initialised before any rank can arrive on it
@@ -702,46 +709,64 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
   }
   __syncthreads();  // the preloaded block-table entries
 
-  // the K and V rows of head g this lane reads from page `entry`: tokens th*8 .. th*8+7
-  const int64_t lane_off = static_cast<int64_t>(th * 8) * kTokenBytes + g * (kHeadDim * 2) + c * 16;
+  auto cp_async16 = [](void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+  };
   auto page_entry = [&](int lp) {
     int e = preload ? s.pages[lp] : bt_row[lp];
     if (e < 0 || e >= p.num_pages) {
-      flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
+      if (lane == 0) flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
       e = 0;
     }
     return e;
   };
-  auto load_page = [&](int e, uint4 (&kr)[8], uint4 (&vr)[8]) {
+  // This warp's pages are p0 + wl, p0 + wl + kWph, ...; its k-th page goes to ring stage
+  // k % kRingStages. Each lane copies (16-byte cp.async) exactly the K and V pieces it reads
+  // later, tokens th*8 .. th*8+7, dims 8c .. 8c+7, into slots of its own, so no lane waits for
+  // another: one commit group per page, and a wait for all but the pages still ahead.
+  const int wl = warp % kWph;
+  const int n_my = p1 - p0 > wl ? (p1 - p0 - wl + kWph - 1) / kWph : 0;
+  const int64_t lane_off = static_cast<int64_t>(th * 8) * kTokenBytes + g * kRowBytes + c * 16;
+  auto slot = [&](int st, int kv, int j) {
+    return s.ring[warp][st][0] + ((kv * 8 + j) * 32 + lane) * 16;
+  };
+  auto issue = [&](int k) {
+    const int e = page_entry(p0 + wl + k * kWph);
+    const int st = k % kRingStages;
     const uint8_t* kp = p.k_pool + static_cast<int64_t>(e) * kPageBytes + lane_off;
     const uint8_t* vp = p.v_pool + static_cast<int64_t>(e) * kPageBytes + lane_off;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) kr[j] = *reinterpret_cast<const uint4*>(kp + j * kTokenBytes);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) vr[j] = *reinterpret_cast<const uint4*>(vp + j * kTokenBytes);
+    for (int j = 0; j < 8; ++j) {
+      cp_async16(slot(st, 0, j), kp + j * kTokenBytes);
+      cp_async16(slot(st, 1, j), vp + j * kTokenBytes);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   };
+  for (int k = 0; k < n_my && k < kRingStages; ++k) issue(k);
 
   float2 acc_a[4], acc_b[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc_a[i] = acc_b[i] = make_float2(0.f, 0.f);
   float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F;  // max used for the exponent, per head
   float l_part = 0.f;                               // this lane's share of its head's sum
-  uint4 kr[8], vr[8];
-  int lp = p0 + warp % kWph;
-  if (lp < p1) load_page(page_entry(lp), kr, vr);
-  for (; lp < p1; lp += kWph) {
+  for (int k = 0; k < n_my; ++k) {
+    const int st = k % kRingStages, lp = p0 + wl + k * kWph;
+    // page k has landed once at most the pages issued after it are still pending
+    const int ahead = min(n_my - 1 - k, kRingStages - 1);
+    if (ahead >= 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else if (ahead == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
     const int n_valid = min(kPage, L - lp * kPage);
-    uint4 nk[8], nv[8];
-    const bool next = lp + kWph < p1;
-    if (next) load_page(page_entry(lp + kWph), nk, nv);
     // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
     float v[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float2 k0 = make_float2(bf16lo(kr[j].x), bf16hi(kr[j].x));
-      const float2 k1 = make_float2(bf16lo(kr[j].y), bf16hi(kr[j].y));
-      const float2 k2 = make_float2(bf16lo(kr[j].z), bf16hi(kr[j].z));
-      const float2 k3 = make_float2(bf16lo(kr[j].w), bf16hi(kr[j].w));
+      const uint4 kr = lds128(slot(st, 0, j));
+      const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
+      const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
+      const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
+      const float2 k3 = make_float2(bf16lo(kr.w), bf16hi(kr.w));
       float2 sa = mul2(qa[0], k0), sb = mul2(qb[0], k0);
       sa = fma2(qa[1], k1, sa); sb = fma2(qb[1], k1, sb);
       sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
@@ -801,25 +826,21 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (th * 8 + j < n_valid) {
+        const uint4 vr = lds128(slot(st, 1, j));
         const float2 ppa = make_float2(pav[j], pav[j]);
         const float2 ppb = make_float2(pbv[j], pbv[j]);
-        const float2 v0 = make_float2(bf16lo(vr[j].x), bf16hi(vr[j].x));
-        const float2 v1 = make_float2(bf16lo(vr[j].y), bf16hi(vr[j].y));
-        const float2 v2 = make_float2(bf16lo(vr[j].z), bf16hi(vr[j].z));
-        const float2 v3 = make_float2(bf16lo(vr[j].w), bf16hi(vr[j].w));
+        const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
+        const float2 v1 = make_float2(bf16lo(vr.y), bf16hi(vr.y));
+        const float2 v2 = make_float2(bf16lo(vr.z), bf16hi(vr.z));
+        const float2 v3 = make_float2(bf16lo(vr.w), bf16hi(vr.w));
         acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
         acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
         acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
         acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
       }
     }
-    if (next) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        kr[j] = nk[j];
-        vr[j] = nv[j];
-      }
-    }
+    // this lane has read its slots of the stage: refill them with the page kRingStages ahead
+    if (k + kRingStages < n_my) issue(k + kRingStages);
   }
 
   // ---- this warp's (m, sum, unnormalised o) per head: lanes 0..15 head 2g, 16..31 head 2g+1
@@ -982,6 +1003,28 @@ DecodePlan decode_plan(int batch, int max_seq_len, int split_tokens, int sm_grid
 // Clusters of decode_cluster_kernel of size C (1, 2, 4 or 8) that the current device can hold
 // at once, from the occupancy calculator (0 if it cannot say: the split path then serves the
 // call); cached per device and size.
+// The single-launch kernels' shared memory is above the 48 KB default: allowed once per device
+// for every instance (under the capacity cache's lock).
+bool configure_small_kernels_locked(int dev) {
+  static bool done[64] = {};
+  if (done[dev]) return true;
+  const int bytes = static_cast<int>(sizeof(SmallSmem));
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<8, 1>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_cluster_kernel<8, 2>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_cluster_kernel<4, 1>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_cluster_kernel<4, 2>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_cluster_kernel<2, 1>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_cluster_kernel<2, 2>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_cluster_kernel<1, 1>, a, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  done[dev] = true;
+  return true;
+}
+
 int small_cluster_capacity(int C, int hpc) {
   static std::mutex mu;
   static int cache[64][2][4];
@@ -990,10 +1033,12 @@ int small_cluster_capacity(int C, int hpc) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int k = C == 1 ? 0 : (C == 2 ? 1 : (C == 4 ? 2 : 3)), h = hpc == 2 ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
+  if (!configure_small_kernels_locked(dev)) return 0;  // the split path serves the call
   if (!known[dev][h][k]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(C * 256));
     cfg.blockDim = dim3(kSmallThreads);
+    cfg.dynamicSmemBytes = sizeof(SmallSmem);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(C);
@@ -1165,7 +1210,7 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(batch) * static_cast<unsigned>(hkv / sp.hpc * C));
       cfg.blockDim = dim3(kSmallThreads);
-      cfg.dynamicSmemBytes = 0;
+      cfg.dynamicSmemBytes = sizeof(SmallSmem);  // allowed by small_path's capacity query
       cfg.stream = st;
       cudaLaunchAttribute attr[2];
       attr[0].id = cudaLaunchAttributeClusterDimension;
