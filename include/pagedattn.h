@@ -125,10 +125,10 @@ pa_status kv_append_paged(pa_dims dims, const void* k_new, const void* v_new, in
  *                workspace must not overlap on the GPU.
  * The key range of all sequences is laid end to end and cut into page ranges (split-KV);
  * partial (o, lse) pairs of sequences that span ranges are merged by log-sum-exp (two
- * kernels). With split_tokens = 0 a short batch (every (sequence, KV head) pair can have a
- * resident cluster of up to 8 CTAs, each holding at most 64 pages) is served by one kernel
- * instead: each pair's cluster splits its pages and merges in distributed shared memory; the
- * workspace is then not touched.
+ * kernels). With split_tokens = 0 a short batch (every (sequence, KV head) pair, or pair of
+ * two KV heads when there are more pairs than SMs, can have a resident cluster of up to 8
+ * CTAs, each holding at most 64 pages) is served by one kernel instead: each cluster splits
+ * its pages and merges in distributed shared memory; the workspace is then not touched.
  * ------------------------------------------------------------------------------------------ */
 size_t pa_decode_workspace_size(pa_dims dims, int32_t batch, int32_t max_seq_len,
                                 int32_t split_tokens);
