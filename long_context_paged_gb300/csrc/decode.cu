@@ -464,12 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
 // each warp takes every kWarps-th partial (a lane holds 4 of the 128 dims) in one online pass
 // with its own running maximum, four partials' loads in flight at a time, and the warps combine
 // through shared memory. When sequences are cut into more partials than 4 warps take in one round
-// (few sequences over many CTAs), 16 warps are used, so that a sequence split over ~64 CTAs is
-// merged in one round of loads.
+// (few sequences over many CTAs), 32 warps are used, so that a sequence split over ~128 CTAs is
+// merged in one round of loads (one sequence over all 152 SMs in two: 16 warps, three rounds,
+// measured 1-2 us slower per call for one long sequence).
 // Launched as a programmatic dependent of decode_splitkv_kernel: its CTAs may start while the
 // split kernel is still running and wait (griddepcontrol.wait) until that grid has completed
 // and its writes are visible, which hides this launch behind the split kernel.
-constexpr int kMergeWarpsSmall = 16, kMergeWarpsLarge = 4;
+constexpr int kMergeWarpsSmall = 32, kMergeWarpsLarge = 4;
 constexpr int kMergePrefixBatch = 64;  // batches this small: page range computed before the wait
 template <int kWarps>
 __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeParams p) {
