@@ -77,6 +77,21 @@ def test_argument_errors_are_rejected_before_launch(lib):
     assert lib.pa_read_device_status(null, null, null) == 1
 
 
+def test_decode_kernels_per_call_query(lib):
+    """pa_decode_kernels_per_call: 0 for unsupported dims or an empty or invalid call, else 1
+    (single-launch path) or 2 (split + merge); explicit split sizes always take the split path.
+    It launches nothing, so it runs without a GPU (where it can only answer 2)."""
+    import long_context_paged_gb300 as pa
+    good = pa.Dims(*pa.DEFAULT_DIMS)
+    assert lib.pa_decode_kernels_per_call(pa.Dims(16, 8, 64, 16), 1, 1000, 0) == 0
+    assert lib.pa_decode_kernels_per_call(good, 0, 1000, 0) == 0
+    assert lib.pa_decode_kernels_per_call(good, 1, -1, 0) == 0
+    assert lib.pa_decode_kernels_per_call(good, 1, 1000, -1) == 0
+    assert lib.pa_decode_kernels_per_call(good, 1, 1000, 0) in (1, 2)
+    assert lib.pa_decode_kernels_per_call(good, 1, 1000, 256) == 2
+    assert lib.pa_decode_kernels_per_call(good, 64, 90000, 0) == 2
+
+
 def test_prefill_argument_errors_are_rejected_before_launch(lib):
     """attn_prefill_chunk's checks, each before any CUDA call. Every case here must be rejected:
     the pointers are fake (aligned, non-null host addresses) and are never dereferenced."""
