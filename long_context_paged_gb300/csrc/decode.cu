@@ -576,16 +576,16 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
 
 // ---------------------------------------------------------------------------------------------
 // Short batches in one launch (decode_cluster_kernel). When every (sequence, KV head) pair of
-// the batch can have a cluster of C CTAs (C a power of two <= 8, batch x Hkv x C <= SMs) and
+// the batch can have a resident cluster of C CTAs (C a power of two <= 8; see small_path) and
 // each CTA then holds few pages, the split above is latency-bound: a prefix pass, a dependent
 // block-table load, one page per SM, partials through L2 and a second kernel that waits for the
 // first to complete. Here CTA rank c of the cluster of pair (b, g) takes pages
-// [cP/C, (c+1)P/C) of sequence b (P = its pages) for KV head g only; its 8 warps take one page
-// each in turn, each warp streaming its pages' K/V rows of head g into its own 3-stage ring
-// (one 256-byte bulk copy per lane and row, two pages in flight ahead of the one computed); the
-// warps combine through shared memory, the ranks write their partial (o, max, sum) into rank 0's
-// shared memory (distributed shared memory of the cluster) and rank 0 merges them and writes
-// the output.
+// [cP/C, (c+1)P/C) of sequence b (P = its pages) for KV head g only (two heads, four warps each,
+// when the batch has more pairs than resident clusters); its warps take one page each in turn,
+// each lane copying its own pieces of the K/V rows of head g into its warp's 3-stage ring
+// (16-byte cp.async, two pages in flight ahead of the one computed); the warps combine through
+// shared memory, the ranks write their partial (o, max, sum) into rank 0's shared memory
+// (distributed shared memory of the cluster) and rank 0 merges them and writes the output.
 // ---------------------------------------------------------------------------------------------
 constexpr int kSmallWarps = 8;
 constexpr int kSmallThreads = kSmallWarps * 32;
@@ -656,8 +656,8 @@ struct SmallSmem {  // dynamic shared memory, 128-byte aligned
   uint64_t full;                             // rank 0: the other ranks' partials have landed
 };
 
-// kHpc KV heads per CTA (1, or 2 when a batch has more (sequence, KV head) pairs than the GPU
-// has SMs): warps w / (8 / kHpc) serve the CTA's head w / (8 / kHpc).
+// kHpc KV heads per CTA (1, or 2 when a batch has more (sequence, KV head) pairs than resident
+// clusters allow): warp w serves the CTA's head w / (8 / kHpc).
 template <int kHkvT, int kHpc>
 __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const DecodeParams p) {
   static_assert(kHpc == 1 || kHpc == 2, "one or two KV heads per CTA");
