@@ -98,6 +98,33 @@ def test_partitioned_decode_of_long_and_empty_sequences(cuda_lib, hk):
     check_attn(out, lse, ref_o, ref_l, what=f"{hk} KV heads, long and empty sequences")
 
 
+@pytest.mark.parametrize("hk,batch", [(4, 48), (2, 88), (1, 100)])
+def test_partitioned_decode_single_launch(cuda_lib, hk, batch):
+    """A device's share of the heads on a short batch goes through the single-launch path: with
+    4 or 2 KV heads these batches have more (sequence, KV head) pairs than the GPU has SMs, so
+    a CTA serves two KV heads; with 1 KV head a CTA per sequence. Checked against the oracle and
+    against the split path (split_tokens=16) on the same inputs."""
+    pa = cuda_lib
+    dims = (2 * hk, hk, W.HEAD_DIM, W.PAGE)
+    rng = np.random.default_rng(hk)
+    lens = [int(x) for x in rng.integers(0, 400, size=batch)]
+    lens[0], lens[1] = 400, 0
+    inp = W.make_paged(95 + hk, lens, [1] * batch, poison=True, device="cuda")
+    kp = inp.k_pools[0][:, :, :hk].contiguous()
+    vp = inp.v_pools[0][:, :, :hk].contiguous()
+    q = inp.q[0][:, :2 * hk].contiguous()
+    assert pa.decode_kernels_per_call(batch, max(lens), dims=dims) == 1
+    ref_o, ref_l = oracle.decode(bits(q), bits(kp), bits(vp), inp.host_block_table,
+                                 inp.host_seq_lens, inp.scale, threads=16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for split in (0, 16):
+        out, lse = pa.attn_decode_paged(q, kp, vp, inp.block_table, inp.seq_lens, max(lens),
+                                        inp.scale, split_tokens=split, status=status, dims=dims)
+        torch.cuda.synchronize()
+        assert pa.read_device_status(status) == 0
+        check_attn(out, lse, ref_o, ref_l, what=f"{hk} KV heads, {batch} sequences, split {split}")
+
+
 def test_unsupported_head_counts_are_rejected(cuda_lib):
     pa = cuda_lib
     inp = W.make_paged(90, [100], [1], device="cuda")
