@@ -31,6 +31,7 @@
 
 #include <mutex>
 
+#include "cluster_common.cuh"
 #include "pa_common.cuh"
 
 namespace pa {
@@ -592,54 +593,6 @@ constexpr int kSmallThreads = kSmallWarps * 32;
 constexpr int kSmallMaxCluster = 8;
 constexpr int kSmallPreload = 256;  // block-table entries loaded beside the length (Pmax <= this)
 constexpr int kSmallMaxPagesPerCta = 64;  // beyond this the full-grid split streams faster
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// every thread of every CTA of the cluster (the barrier inits are visible after it)
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// address of the same shared-memory location in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-// arrive on an mbarrier of another CTA of the cluster, ordering this thread's earlier writes
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-               : "memory");
-}
-// bounded wait that also acquires writes made by other CTAs of the cluster
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
-                                                          uint64_t limit_ns) {
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    if (i == 0) t0 = global_timer_ns();
-    else if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
 
 constexpr int kRingStages = 3;                  // pages in flight per warp (incl. the current)
 constexpr int kRowBytes = kHeadDim * 2;         // one token's row of one head
