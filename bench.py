@@ -534,7 +534,7 @@ def main():
                               "sample": res["prefill"]["sample"]}
 
     # roofline of the dominant kernel (by device time), the other one alongside
-    dec_src = source_hash("decode.cu", "pa_common.cuh")
+    dec_src = source_hash("decode.cu", "pa_common.cuh", "cluster_common.cuh")
     pf_src = source_hash("prefill_tc.cu", "tc_common.cuh", "pa_common.cuh")
     roofs = []
     if t_dec:
