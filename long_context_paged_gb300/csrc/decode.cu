@@ -466,26 +466,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
 // with its own running maximum, four partials' loads in flight at a time, and the warps combine
 // through shared memory. When sequences are cut into more partials than 4 warps take in one round
 // (few sequences over many CTAs), 32 warps are used, so that a sequence split over ~128 CTAs is
-// merged in one round of loads (one sequence over all 152 SMs in two: 16 warps, three rounds,
-// measured 1-2 us slower per call for one long sequence).
+// merged in one round of loads (16 warps, three rounds for one sequence over all 152 SMs,
+// measured 1-2 us slower per call); beyond 64 partials decode_merge_dims_kernel takes over.
 // Launched as a programmatic dependent of decode_splitkv_kernel: its CTAs may start while the
 // split kernel is still running and wait (griddepcontrol.wait) until that grid has completed
 // and its writes are visible, which hides this launch behind the split kernel.
 constexpr int kMergeWarpsSmall = 32, kMergeWarpsLarge = 4;
 constexpr int kMergePrefixBatch = 64;  // batches this small: page range computed before the wait
-template <int kWarps>
-__global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeParams p) {
-  // the next kernel on the stream may launch now; it waits for this grid before reading anything
-  asm volatile("griddepcontrol.launch_dependents;");
-  __shared__ float red_m[kWarps], red_w[kWarps];
-  __shared__ float4 red_o[kWarps][32];
-  const int b = blockIdx.x, h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hq = p.hq, slots = p.stage_pages;
-  // For a small batch every warp computes this sequence's page range and the split's range size
-  // from the lengths, with the split kernel's own arithmetic, while the split kernel still runs;
-  // a large batch reads them from the workspace after the wait.
-  int p0 = 0, p1 = 0, W = 0;
+
+// Sequence b's first and past-last global page and the split's range size W, as the split kernel
+// computed them. For a small batch every warp derives them from the lengths with the split
+// kernel's own arithmetic while the split kernel still runs; a large batch reads them from the
+// workspace after the wait. Contains the grid dependency wait.
+__device__ __forceinline__ void merge_seq_range(const DecodeParams& p, int b, int lane, int& p0,
+                                                int& p1, int& W) {
+  p0 = p1 = W = 0;
   const bool early = p.batch <= kMergePrefixBatch;
   if (early) {
     const int n0 = lane < p.batch ? (clamp_len(p, lane, false) + kPage - 1) / kPage : 0;
@@ -506,7 +501,21 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
   if (!early) {
     p0 = p.ws_prefix[b];
     p1 = p.ws_prefix[b + 1];
+    W = p.ws_header[0];
   }
+}
+
+template <int kWarps>
+__global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeParams p) {
+  // the next kernel on the stream may launch now; it waits for this grid before reading anything
+  asm volatile("griddepcontrol.launch_dependents;");
+  __shared__ float red_m[kWarps], red_w[kWarps];
+  __shared__ float4 red_o[kWarps][32];
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq = p.hq, slots = p.stage_pages;
+  int p0, p1, W;
+  merge_seq_range(p, b, lane, p0, p1, W);
   uint16_t* orow = p.out + (static_cast<int64_t>(b) * hq + h) * kHeadDim + 4 * lane;
   if (p1 == p0) {
     if (warp == 0) {
@@ -515,7 +524,6 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
     }
     return;
   }
-  if (!early) W = p.ws_header[0];
   const int r0 = p0 / W, r1 = (p1 - 1) / W;
   if (r0 == r1 && slots == 1) return;  // finished inside one CTA
   // partials c0 .. c1: record b * slots + c, c = range * slots + page slot
@@ -573,6 +581,83 @@ __global__ void __launch_bounds__(kWarps * 32) decode_merge_kernel(const DecodeP
   *reinterpret_cast<uint2*>(orow) =
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
   if (lane == 0 && p.lse != nullptr) p.lse[b * hq + h] = (M + log2f(wsum)) * kLn2;
+}
+
+// The same merge for sequences cut into many partials (more than 64: a few sequences over all
+// SMs). Each head's 128 dims are split over kMergeDimParts CTAs of 32 warps, a lane holding one
+// dim, so a CTA reads 32 dims of every partial (a quarter of what one CTA per head would), and
+// each warp keeps eight partials' loads in flight: up to 256 partials in one round of loads.
+constexpr int kMergeDimParts = 4;
+constexpr int kMergeManyPartials = 64;
+__global__ void __launch_bounds__(kMergeWarpsSmall * 32) decode_merge_dims_kernel(const DecodeParams p) {
+  constexpr int kWarps = kMergeWarpsSmall, kInFlight = 8;
+  asm volatile("griddepcontrol.launch_dependents;");
+  __shared__ float red_m[kWarps], red_w[kWarps];
+  __shared__ float red_o[kWarps][32];
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = blockIdx.z * 32 + lane;  // this lane's dim
+  const int hq = p.hq, slots = p.stage_pages;
+  int p0, p1, W;
+  merge_seq_range(p, b, lane, p0, p1, W);
+  uint16_t* orow = p.out + (static_cast<int64_t>(b) * hq + h) * kHeadDim;
+  if (p1 == p0) {
+    if (warp == 0) {
+      orow[d] = 0;
+      if (blockIdx.z == 0 && lane == 0 && p.lse != nullptr) p.lse[b * hq + h] = -CUDART_INF_F;
+    }
+    return;
+  }
+  const int r0 = p0 / W, r1 = (p1 - 1) / W;
+  if (r0 == r1 && slots == 1) return;  // finished inside one CTA
+  const int c0 = r0 * slots, c1 = r1 * slots + slots - 1;
+  const float* lse_src = p.ws_lse + static_cast<int64_t>(b) * slots * hq + h;
+  const float* o_src = p.ws_o + (static_cast<int64_t>(b) * slots * hq + h) * kHeadDim + d;
+  float m = -CUDART_INF_F, wsum = 0.f, acc = 0.f;
+  for (int c = c0 + warp; c <= c1; c += kInFlight * kWarps) {
+    float l2[kInFlight], o[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int cu = c + u * kWarps;
+      l2[u] = cu <= c1 ? lse_src[static_cast<int64_t>(cu) * hq] * kLog2e : -CUDART_INF_F;
+      o[u] = cu <= c1 ? o_src[static_cast<int64_t>(cu) * hq * kHeadDim] : 0.f;
+    }
+    float mn = m;
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) mn = fmaxf(mn, l2[u]);
+    const float ms = mn == -CUDART_INF_F ? 0.f : mn;  // no finite partial yet: weights all 0
+    const float sc = fast_exp2(m - ms);
+    acc *= sc;
+    wsum *= sc;
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const float w = fast_exp2(l2[u] - ms);
+      wsum += w;
+      acc += w * o[u];
+    }
+    m = mn;
+  }
+  red_o[warp][lane] = acc;
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_w[warp] = wsum;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float M = red_m[0];
+#pragma unroll
+  for (int k = 1; k < kWarps; ++k) M = fmaxf(M, red_m[k]);
+  const float Ms = M == -CUDART_INF_F ? 0.f : M;
+  float a = 0.f;
+  wsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < kWarps; ++k) {
+    const float sk = fast_exp2(red_m[k] - Ms);  // a warp with no partial has m = -inf: s = 0
+    a += sk * red_o[k][lane];
+    wsum += sk * red_w[k];
+  }
+  orow[d] = static_cast<uint16_t>(pack_bf16x2(a / wsum, 0.f) & 0xffffu);
+  if (blockIdx.z == 0 && lane == 0 && p.lse != nullptr) p.lse[b * hq + h] = (M + log2f(wsum)) * kLn2;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1125,6 +1210,9 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
       e = cudaFuncSetAttribute(decode_merge_kernel<kMergeWarpsLarge>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_merge_dims_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return record_cuda_error(e, "cudaFuncSetAttribute(decode merge)");
     configured_device = dev;
   }
@@ -1217,9 +1305,10 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
     // partials per sequence when the lengths are equal: ceil(ranges / batch), plus one for a
     // cut at each end, times the page slots per range; more than 4 warps take in one round of
     // 4 loads -> 16 warps per head
-    const bool small =
-        ((plan.max_ranges + batch - 1) / batch + 1) * p.stage_pages > 4 * kMergeWarpsLarge;
-    cfg.gridDim = dim3(batch, dims.num_q_heads);
+    const int partials = ((plan.max_ranges + batch - 1) / batch + 1) * p.stage_pages;
+    const bool many = partials > kMergeManyPartials;
+    const bool small = partials > 4 * kMergeWarpsLarge;
+    cfg.gridDim = dim3(batch, dims.num_q_heads, many ? kMergeDimParts : 1);
     cfg.blockDim = dim3((small ? kMergeWarpsSmall : kMergeWarpsLarge) * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -1228,7 +1317,8 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = small ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<kMergeWarpsSmall>, p)
+    cudaError_t e = many ? cudaLaunchKernelEx(&cfg, decode_merge_dims_kernel, p)
+                  : small ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<kMergeWarpsSmall>, p)
                           : cudaLaunchKernelEx(&cfg, decode_merge_kernel<kMergeWarpsLarge>, p);
     if (e != cudaSuccess) return record_cuda_error(e, "decode_merge_kernel");
   }
