@@ -1,6 +1,6 @@
 // Thread-block-cluster helpers (PTX ISA: %cluster_ctarank, barrier.cluster, mapa,
 // st.shared::cluster, mbarrier with cluster scope) shared by the kernels that exchange data
-// through distributed shared memory. No multicast: each store and arrive targets one CTA.
+// through distributed shared memory. Each store and each arrive targets exactly one CTA.
 #pragma once
 
 #include <stdint.h>
