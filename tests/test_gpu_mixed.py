@@ -69,8 +69,8 @@ def chunk_rows_256(n, rng):
 def test_mixed_step_full_size(cuda_lib):
     """The 28-layer mixed workload at full size (about 173 GB of pools), in the bench's launch
     configuration: on layers 0 and 27 and two more drawn by seed, every decode sequence and
-    256 rows of the chunk (every head) are checked against the oracle, which appends the new
-    tokens itself into the pools as they were before the step."""
+    256 rows of the chunk (every head; on layer 0 all 4,096 rows) are checked against the oracle,
+    which appends the new tokens itself into the pools as they were before the step."""
     free, _ = torch.cuda.mem_get_info()
     L, ql = W.lengths_for("mixed_28l")
     need = 28 * 2 * int((-(-L // 16)).sum() + 16) * 32768 + (8 << 30)
@@ -90,7 +90,10 @@ def test_mixed_step_full_size(cuda_lib):
     assert len(rows) == 256
     for layer in sorted(check_layers):
         kb, vb = saved.pop(layer)
-        ro = oracle_mixed(inp, layer, kb, vb, 4096, prefill_rows=rows)
+        # layer 0: every row of the chunk; the others: the 256 sampled rows
+        layer_rows = None if layer == 0 else rows
+        ro = oracle_mixed(inp, layer, kb, vb, 4096, prefill_rows=layer_rows)
         po, pl, do, dl = outs[layer]
-        check_attn(po, pl, ro[0], ro[1], rows=rows, what=f"layer {layer} prefill")
+        check_attn(po, pl, ro[0], ro[1], rows=layer_rows,
+                   what=f"layer {layer} prefill ({'all 4,096 rows' if layer_rows is None else '256 rows'})")
         check_attn(do, dl, ro[2], ro[3], what=f"layer {layer} decode (all 31 sequences)")
