@@ -221,15 +221,35 @@ class Step:
         self.launches_per_step = self.layers * ((1 if self.append else 0) + (2 if self.n_chunk_rows else 0)
                                                 + self.dec_kernels)
 
-    def run(self, events=None, q_src=None, parts=("append", "prefill", "decode")):
+    def run(self, events=None, q_src=None, parts=("append", "prefill", "decode"), split=None):
+        """One pass over the layers. split = (prefill CTAs, decode CTAs): after each layer's append,
+        the decode runs on a second stream beside the prefill, each call's persistent grid capped
+        at its share of the SMs, and the first stream waits for it before the next layer."""
         pa, inp = self.pa, self.inp
         stream = torch.cuda.current_stream()
+        both = split is not None and self.n_chunk_rows and len(self.dec_idx) \
+            and "prefill" in parts and "decode" in parts
+        if both and not hasattr(self, "side"):
+            self.side = torch.cuda.Stream(device=self.dev)
         for layer in range(self.layers):
             q = inp.q[layer] if q_src is None else q_src[layer]
             if self.append and "append" in parts:
                 pa.kv_append_paged(inp.k_new[layer], inp.v_new[layer], inp.cu_q_lens, inp.start_pos,
                                    inp.block_table, inp.k_pools[layer], inp.v_pools[layer],
                                    status=self.status, stream=stream)
+            if both:
+                self.side.wait_stream(stream)
+                pa.attn_prefill_chunk(q[:self.n_chunk_rows], self.pf_cu, inp.k_pools[layer],
+                                      inp.v_pools[layer], self.pf_bt, self.pf_sl, self.n_chunk_rows,
+                                      self.max_s, inp.scale, out=self.pf_out, lse=self.pf_lse,
+                                      workspace=self.pf_ws, status=self.status, stream=stream,
+                                      max_ctas=split[0])
+                pa.attn_decode_paged(q[self.n_chunk_rows:], inp.k_pools[layer], inp.v_pools[layer],
+                                     self.dec_bt, self.dec_sl, self.max_s, inp.scale,
+                                     out=self.dec_out, lse=self.dec_lse, workspace=self.ws,
+                                     status=self.status, stream=self.side, max_ctas=split[1])
+                stream.wait_stream(self.side)
+                continue
             if self.n_chunk_rows and "prefill" in parts:
                 if events is not None:
                     events["pf"][layer][0].record(stream)
@@ -398,10 +418,10 @@ def cpu_baseline(step: Step, budget_s: float = 10.0, prefill_budget_s: float = 4
 # CUDA-graph replay: the C-ABI calls are capture-safe (grids from host bounds, no host sync),
 # so each timed phase is captured once and replayed; the device time then has no host gaps.
 # ----------------------------------------------------------------------------------------------
-def capture(step: Step, parts):
+def capture(step: Step, parts, split=None):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        step.run(parts=parts)
+        step.run(parts=parts, split=split)
     return g
 
 
@@ -453,6 +473,10 @@ def main():
     ap.add_argument("--no-buckets", action="store_true",
                     help="skip the decode batch-bucket latencies added to the default line")
     ap.add_argument("--clocks-out", default=None)
+    ap.add_argument("--decode-ctas", type=int, default=-1,
+                    help="whole-step graph: CTAs of each layer's decode, run on a second stream "
+                         "beside the prefill on the other SMs (-1: 47%% of the SMs; 0: one after "
+                         "the other)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -485,7 +509,15 @@ def main():
     if flags:
         raise RuntimeError(f"device status flagged errors in the first pass: {flags}")
     has_dec, has_pf = len(step.dec_idx) > 0, step.n_chunk_rows > 0
-    g_step = capture(step, ("append", "prefill", "decode"))
+    # The whole step: after each layer's append, the chunk's prefill (tensor-bound) and the
+    # decode batch (HBM-bound) run side by side on disjoint SMs; the per-mode graphs below keep
+    # each call alone on the whole GPU (that is where the decode and prefill rates come from).
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    step_split = None
+    if has_dec and has_pf and args.decode_ctas != 0:
+        nd = round(0.47 * sms) if args.decode_ctas < 0 else min(args.decode_ctas, sms - 1)
+        step_split = (sms - nd, nd)
+    g_step = capture(step, ("append", "prefill", "decode"), split=step_split)
     g_dec = capture(step, ("decode",)) if has_dec else None
     g_pf = capture(step, ("prefill",)) if has_pf and has_dec else None
 
@@ -587,7 +619,11 @@ def main():
                    "l2": "inputs larger than L2 (each step reads every layer's pools)",
                    "timing": "CUDA events around K CUDA-graph replays each of: the whole step "
                              "(ms_per_step), its decode calls only (decode GB/s), its prefill "
-                             "calls only (prefill TFLOP/s)"},
+                             "calls only (prefill TFLOP/s)",
+                   "step_overlap": None if step_split is None else
+                   {"prefill_ctas": step_split[0], "decode_ctas": step_split[1],
+                    "how": "per layer, after kv_append: prefill and decode on two streams, "
+                           "each call's persistent grid capped at its share of the SMs"}},
         "phase_ms_per_step": {"step": round(total_s * 1e3 / K_, 3),
                               "decode": round(t_dec * 1e3 / K_, 3) if t_dec else None,
                               "prefill": round(t_pf * 1e3 / K_, 3) if t_pf else None},

@@ -212,6 +212,47 @@ pa_status attn_prefill_chunk(pa_dims dims, const void* q, const int32_t* cu_q_le
                              pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * attn_decode_paged_ex / attn_prefill_chunk_ex — the two attention calls with a grid cap.
+ *
+ * Source: the serving pages' scheduler runs a prompt chunk and other requests' decode steps in
+ * the same step ("Optimizing ASR Models to Transcribe 90-Minute Multi-Speaker Audio", section
+ * "Chunked Prefill for Long Audio"). The chunk's attention is bound by the tensor cores and the
+ * decodes' by HBM bandwidth, so a caller can run the two side by side, on two streams, each
+ * call held to its own share of the SMs: the two bounds then overlap instead of adding up.
+ *
+ * The arguments are those of attn_decode_paged / attn_prefill_chunk plus opts (NULL = the
+ * plain call):
+ *   opts->max_ctas  > 0: the call's persistent grid has at most this many CTAs (each occupies
+ *                   one SM); 0: one per SM, as the plain call; < 0: PA_ERR_INVALID_ARG.
+ *                   The workspace sizes of the plain calls cover every cap. A decode batch
+ *                   that the single-launch path would serve takes it only if its CTAs fit
+ *                   under the cap, else the split path runs with the capped grid.
+ * Results equal the plain call's up to rounding (a smaller grid cuts the key ranges
+ * differently). Ordering between the two streams is the caller's (e.g. an event recorded after
+ * kv_append_paged, waited on by the second stream, and one recorded on the second stream after
+ * its call, waited on by the first before the next layer); all of it can be captured in one
+ * CUDA graph.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  int32_t max_ctas;
+} pa_launch_opts;
+
+pa_status attn_decode_paged_ex(pa_dims dims, const void* q, const void* k_pool,
+                               const void* v_pool, int64_t num_pages, const int32_t* block_table,
+                               int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
+                               int32_t max_seq_len, float softmax_scale, int32_t split_tokens,
+                               void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               int32_t* status, pa_stream_t stream, const pa_launch_opts* opts);
+
+pa_status attn_prefill_chunk_ex(pa_dims dims, const void* q, const int32_t* cu_q_lens,
+                                int32_t total_q, const void* k_pool, const void* v_pool,
+                                int64_t num_pages, const int32_t* block_table, int32_t bt_stride,
+                                const int32_t* seq_lens, int32_t batch, int32_t max_q_len,
+                                int32_t max_seq_len, float softmax_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                pa_stream_t stream, const pa_launch_opts* opts);
+
+/* ------------------------------------------------------------------------------------------
  * attn_merge_lse — combine attention results computed over disjoint key sets.
  *
  * Source: the split-KV form of the decode step (long caches are cut into key ranges whose

@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "load", "PagedAttnError", "Dims", "DEFAULT_DIMS",
     "kv_append_paged", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_prefill_chunk",
-    "attn_merge_lse", "adaptor_mlp_merge4", "adaptor_workspace_size",
+    "attn_merge_lse", "adaptor_mlp_merge4", "adaptor_workspace_size", "LaunchOpts",
     "decode_workspace_size", "decode_kernels_per_call", "prefill_workspace_size",
     "read_device_status", "debug_decode_starve",
     "DEV_ERR_PAGE_OOB", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "DEV_ERR_INTERNAL", "lib_path",
@@ -63,6 +63,21 @@ _I64 = ctypes.c_int64
 _SZ = ctypes.c_size_t
 _F = ctypes.c_float
 
+class LaunchOpts(ctypes.Structure):
+    """pa_launch_opts: max_ctas > 0 caps a call's persistent grid (0 = one CTA per SM)."""
+    _fields_ = [("max_ctas", ctypes.c_int32)]
+
+
+def _opts(max_ctas):
+    if max_ctas is None:
+        return None, None
+    m = int(max_ctas)
+    if m < 0:
+        raise ValueError("max_ctas must be >= 0")
+    o = LaunchOpts(m)
+    return o, ctypes.byref(o)
+
+
 _SIGS = {
     "kv_append_paged": (_I32, [Dims, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _I64, _P, _P]),
     "pa_decode_workspace_size": (_SZ, [Dims, _I32, _I32, _I32]),
@@ -75,6 +90,10 @@ _SIGS = {
     "pa_prefill_workspace_size": (_SZ, [Dims, _I32, _I32, _I32]),
     "attn_prefill_chunk": (_I32, [Dims, _P, _P, _I32, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
                                   _F, _P, _P, _P, _SZ, _P, _P]),
+    "attn_decode_paged_ex": (_I32, [Dims, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _F, _I32, _P,
+                                    _P, _P, _SZ, _P, _P, _P]),
+    "attn_prefill_chunk_ex": (_I32, [Dims, _P, _P, _I32, _P, _P, _I64, _P, _I32, _P, _I32, _I32,
+                                     _I32, _F, _P, _P, _P, _SZ, _P, _P, _P]),
     "attn_merge_lse": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "pa_adaptor_workspace_size": (_SZ, [_I32]),
     "adaptor_mlp_merge4": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _SZ, _P, _P]),
@@ -234,10 +253,12 @@ def _workspace(nbytes, device, workspace):
 
 def attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int,
                       softmax_scale: float, *, split_tokens: int = 0, out=None, lse=None,
-                      workspace=None, status=None, stream=None, want_lse=True, dims=None):
+                      workspace=None, status=None, stream=None, want_lse=True, dims=None,
+                      max_ctas=None):
     """Decode attention: q [B, Hq, D] over each sequence's cached keys. Returns (out, lse).
 
-    split_tokens: keys per split-KV range (whole pages); 0 = one equal share per SM."""
+    split_tokens: keys per split-KV range (whole pages); 0 = one equal share per SM.
+    max_ctas: cap on the persistent grid (attn_decode_paged_ex); None = the plain call."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_pool, "k_pool", torch.bfloat16, 4)
     _need(v_pool, "v_pool", torch.bfloat16, 4)
@@ -263,11 +284,16 @@ def attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int
     _on_device("attn_decode_paged", q, k_pool, v_pool, block_table, seq_lens, out, lse,
                workspace, status)
     lib = load()
-    _check("attn_decode_paged", lib.attn_decode_paged(
-        _dims(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
-        block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), float(softmax_scale),
-        int(split_tokens), _ptr(out), _ptr(lse), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+    args = (_dims(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), float(softmax_scale),
+            int(split_tokens), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    keep, ref = _opts(max_ctas)
+    if ref is None:
+        _check("attn_decode_paged", lib.attn_decode_paged(*args))
+    else:
+        _check("attn_decode_paged_ex", lib.attn_decode_paged_ex(*args, ref))
+    del keep
     return out, lse
 
 
@@ -308,8 +334,11 @@ def attn_decode_paged_noalloc(q, k_pool, v_pool, block_table, seq_lens, max_seq_
 
 def attn_prefill_chunk(q, cu_q_lens, k_pool, v_pool, block_table, seq_lens, max_q_len: int,
                        max_seq_len: int, softmax_scale: float, *, out=None, lse=None,
-                       workspace=None, status=None, stream=None, want_lse=True, dims=None):
-    """Chunked prefill: q [Tq, Hq, D] packed by cu_q_lens. Returns (out, lse)."""
+                       workspace=None, status=None, stream=None, want_lse=True, dims=None,
+                       max_ctas=None):
+    """Chunked prefill: q [Tq, Hq, D] packed by cu_q_lens. Returns (out, lse).
+
+    max_ctas: cap on the persistent grid (attn_prefill_chunk_ex); None = the plain call."""
     _need(q, "q", torch.bfloat16, 3)
     _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
     _need(k_pool, "k_pool", torch.bfloat16, 4)
@@ -338,12 +367,18 @@ def attn_prefill_chunk(q, cu_q_lens, k_pool, v_pool, block_table, seq_lens, max_
     _on_device("attn_prefill_chunk", q, cu_q_lens, k_pool, v_pool, block_table, seq_lens, out,
                lse, workspace, status)
     lib = load()
-    _check("attn_prefill_chunk", lib.attn_prefill_chunk(
-        _dims(dims), _ptr(q), _ptr(cu_q_lens), q.shape[0], _ptr(k_pool), _ptr(v_pool),
-        k_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
-        int(max_q_len), int(max_seq_len), float(softmax_scale), _ptr(out), _ptr(lse),
-        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
-        _ptr(status), _stream(stream)))
+    args = (_dims(dims), _ptr(q), _ptr(cu_q_lens), q.shape[0], _ptr(k_pool), _ptr(v_pool),
+            k_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+            int(max_q_len), int(max_seq_len), float(softmax_scale), _ptr(out), _ptr(lse),
+            _ptr(workspace),
+            0 if workspace is None else workspace.numel() * workspace.element_size(),
+            _ptr(status), _stream(stream))
+    keep, ref = _opts(max_ctas)
+    if ref is None:
+        _check("attn_prefill_chunk", lib.attn_prefill_chunk(*args))
+    else:
+        _check("attn_prefill_chunk_ex", lib.attn_prefill_chunk_ex(*args, ref))
+    del keep
     return out, lse
 
 

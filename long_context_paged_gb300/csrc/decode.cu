@@ -1160,15 +1160,15 @@ extern "C" int32_t pa_decode_kernels_per_call(pa_dims dims, int32_t batch, int32
   return pa::small_path(dims.num_kv_heads, batch, max_seq_len, split_tokens).C > 0 ? 1 : 2;
 }
 
-extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool,
-                                       const void* v_pool, int64_t num_pages,
-                                       const int32_t* block_table, int32_t bt_stride,
-                                       const int32_t* seq_lens, int32_t batch,
-                                       int32_t max_seq_len, float softmax_scale,
-                                       int32_t split_tokens, void* out, float* lse,
-                                       void* workspace, size_t workspace_bytes, int32_t* status,
-                                       pa_stream_t stream) {
-  using namespace pa;
+namespace pa {
+namespace {
+// attn_decode_paged with a cap on the grid (max_ctas > 0; 0 = one CTA per SM)
+pa_status decode_call(pa_dims dims, const void* q, const void* k_pool, const void* v_pool,
+                      int64_t num_pages, const int32_t* block_table, int32_t bt_stride,
+                      const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                      float softmax_scale, int32_t split_tokens, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int32_t* status,
+                      pa_stream_t stream, int32_t max_ctas) {
   if (!gqa_dims_supported(dims)) return PA_ERR_UNSUPPORTED;
   if (batch < 0 || batch > kMaxBatch || bt_stride <= 0 || num_pages <= 0 || max_seq_len < 0 ||
       max_seq_len > 131072 || !(softmax_scale == softmax_scale) || split_tokens < 0)
@@ -1180,8 +1180,9 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
        reinterpret_cast<uintptr_t>(v_pool) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return PA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
-  const int sm_grid = decode_grid_size();
-  if (sm_grid <= 0) return PA_ERR_CUDA;
+  const int full_grid = decode_grid_size();
+  if (full_grid <= 0) return PA_ERR_CUDA;
+  const int sm_grid = max_ctas > 0 ? std::min(full_grid, static_cast<int>(max_ctas)) : full_grid;
   const DecodePlan plan = decode_plan(batch, max_seq_len, split_tokens, sm_grid);
   const int hkv = dims.num_kv_heads;
   if (workspace_bytes < ws_layout(batch, plan.ws_ranges, hkv).total) return PA_ERR_WORKSPACE_TOO_SMALL;
@@ -1247,7 +1248,7 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
   // Short batches in one launch (decode_cluster_kernel; see small_path)
   {
     const SmallPath sp = small_path(hkv, batch, max_seq_len, split_tokens);
-    if (sp.C > 0) {
+    if (sp.C > 0 && (max_ctas <= 0 || static_cast<int64_t>(batch) * (hkv / sp.hpc * sp.C) <= max_ctas)) {
       const int C = sp.C;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(batch) * static_cast<unsigned>(hkv / sp.hpc * C));
@@ -1323,6 +1324,38 @@ extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* 
     if (e != cudaSuccess) return record_cuda_error(e, "decode_merge_kernel");
   }
   return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status attn_decode_paged(pa_dims dims, const void* q, const void* k_pool,
+                                       const void* v_pool, int64_t num_pages,
+                                       const int32_t* block_table, int32_t bt_stride,
+                                       const int32_t* seq_lens, int32_t batch,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       int32_t split_tokens, void* out, float* lse,
+                                       void* workspace, size_t workspace_bytes, int32_t* status,
+                                       pa_stream_t stream) {
+  return pa::decode_call(dims, q, k_pool, v_pool, num_pages, block_table, bt_stride, seq_lens,
+                         batch, max_seq_len, softmax_scale, split_tokens, out, lse, workspace,
+                         workspace_bytes, status, stream, 0);
+}
+
+extern "C" pa_status attn_decode_paged_ex(pa_dims dims, const void* q, const void* k_pool,
+                                          const void* v_pool, int64_t num_pages,
+                                          const int32_t* block_table, int32_t bt_stride,
+                                          const int32_t* seq_lens, int32_t batch,
+                                          int32_t max_seq_len, float softmax_scale,
+                                          int32_t split_tokens, void* out, float* lse,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t* status, pa_stream_t stream,
+                                          const pa_launch_opts* opts) {
+  const int32_t cap = opts != nullptr ? opts->max_ctas : 0;
+  if (cap < 0) return PA_ERR_INVALID_ARG;
+  return pa::decode_call(dims, q, k_pool, v_pool, num_pages, block_table, bt_stride, seq_lens,
+                         batch, max_seq_len, softmax_scale, split_tokens, out, lse, workspace,
+                         workspace_bytes, status, stream, cap);
 }
 
 // ---------------------------------------------------------------------------------------------

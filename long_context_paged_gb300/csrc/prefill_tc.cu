@@ -1066,14 +1066,17 @@ pa_status launch_prefill_tc(int32_t hkv, const void* q, int32_t total_q, const i
                             const int32_t* block_table, int32_t bt_stride,
                             const int32_t* seq_lens, int32_t batch, int32_t max_q_len,
                             float softmax_scale, void* out, float* lse, void* workspace,
-                            size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
+                            size_t workspace_bytes, int32_t* status, cudaStream_t stream,
+                            int32_t max_ctas) {
   if (batch > kMaxBatch) {
     snprintf_error("attn_prefill_chunk: at most %d chunks per call", kMaxBatch);
     return PA_ERR_UNSUPPORTED;
   }
   if (num_pages * kPage >= (int64_t(1) << 31) || total_q >= (1 << 24)) return PA_ERR_UNSUPPORTED;
-  const int grid = prefill_grid();
-  if (grid <= 0) return PA_ERR_CUDA;
+  const int full_grid = prefill_grid();
+  if (full_grid <= 0) return PA_ERR_CUDA;
+  // one persistent CTA per SM, or fewer when the caller caps the grid (the plan adapts to it)
+  const int grid = max_ctas > 0 ? std::min(full_grid, static_cast<int>(max_ctas)) : full_grid;
   const PrefillWs w = prefill_ws(batch, grid);
   if (workspace == nullptr || workspace_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;

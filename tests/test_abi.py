@@ -203,3 +203,26 @@ def test_adaptor_argument_errors_are_rejected_before_launch(lib):
     assert need == 2 * 1024 * 2 + 256                    # bf16 hidden rows of the 2 merged tokens
     assert call(8, ws_bytes=need - 1) == 3               # workspace too small
     assert lib.pa_adaptor_workspace_size(-1) == 0
+
+
+def test_grid_cap_argument_errors_are_rejected_before_launch(lib):
+    """attn_decode_paged_ex / attn_prefill_chunk_ex: a negative max_ctas is an argument error,
+    returned before any CUDA call (so this runs without a GPU)."""
+    import long_context_paged_gb300 as pa
+    good = pa.Dims(16, 8, 128, 16)
+    null = None
+    bad = pa.LaunchOpts(-1)
+    assert lib.attn_decode_paged_ex(good, null, null, null, 1, null, 1, null, 1, 16, 1.0, 0,
+                                    null, null, null, 0, null, null, ctypes.byref(bad)) == 1
+    assert lib.attn_prefill_chunk_ex(good, null, null, 1, null, null, 1, null, 1, null, 1, 1, 16,
+                                     1.0, null, null, null, 0, null, null, ctypes.byref(bad)) == 1
+    # unsupported head shapes stay PA_ERR_UNSUPPORTED whatever the cap
+    ok = pa.LaunchOpts(8)
+    assert lib.attn_decode_paged_ex(pa.Dims(16, 8, 64, 16), null, null, null, 1, null, 1, null, 1,
+                                    16, 1.0, 0, null, null, null, 0, null, null,
+                                    ctypes.byref(ok)) == 2
+    assert lib.attn_prefill_chunk_ex(pa.Dims(16, 4, 128, 16), null, null, 1, null, null, 1, null,
+                                     1, null, 1, 1, 16, 1.0, null, null, null, 0, null, null,
+                                     ctypes.byref(ok)) == 2
+    with pytest.raises(ValueError):
+        pa._opts(-2)

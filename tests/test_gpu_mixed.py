@@ -97,3 +97,59 @@ def test_mixed_step_full_size(cuda_lib):
         check_attn(po, pl, ro[0], ro[1], rows=layer_rows,
                    what=f"layer {layer} prefill ({'all 4,096 rows' if layer_rows is None else '256 rows'})")
         check_attn(do, dl, ro[2], ro[3], what=f"layer {layer} decode (all 31 sequences)")
+
+
+@pytest.mark.parametrize("split", [(80, 72), (120, 32), (8, 144)])
+def test_mixed_step_overlapped_on_two_streams(cuda_lib, split):
+    """The bench's whole-step form: after each layer's append, the prefill runs on the current
+    stream with its grid capped at split[0] CTAs and the decode on a second stream capped at
+    split[1], both captured in one CUDA graph and replayed; every row checked against the
+    oracle (reduced sizes, two layers)."""
+    dec = [500, 9000, 1234, 16, 4097, 7777, 31]
+    inp = W.make_paged(400, [2048 + 256] + dec, [256] + [1] * 7, layers=2, device="cuda")
+    kb = [bits(inp.k_pools[l]).copy() for l in range(2)]
+    vb = [bits(inp.v_pools[l]).copy() for l in range(2)]
+    max_s = int(inp.host_seq_lens.max())
+    dev = inp.q[0].device
+    side = torch.cuda.Stream(device=dev)
+    outs = [(torch.empty(256, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev),
+             torch.empty(256, W.HQ, dtype=torch.float32, device=dev),
+             torch.empty(7, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev),
+             torch.empty(7, W.HQ, dtype=torch.float32, device=dev)) for _ in range(2)]
+    dws = torch.empty(cuda_lib.decode_workspace_size(7, max_s), dtype=torch.uint8, device=dev)
+    pws = torch.empty(max(256, cuda_lib.prefill_workspace_size(1, 256, max_s)), dtype=torch.uint8,
+                      device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        stream = torch.cuda.current_stream()
+        for layer in range(2):
+            cuda_lib.kv_append_paged(inp.k_new[layer], inp.v_new[layer], inp.cu_q_lens,
+                                     inp.start_pos, inp.block_table, inp.k_pools[layer],
+                                     inp.v_pools[layer], status=status, stream=stream)
+            side.wait_stream(stream)
+            po, pl, do, dl = outs[layer]
+            q = inp.q[layer]
+            cuda_lib.attn_prefill_chunk(q[:256], inp.cu_q_lens[:2], inp.k_pools[layer],
+                                        inp.v_pools[layer], inp.block_table[:1], inp.seq_lens[:1],
+                                        256, max_s, inp.scale, out=po, lse=pl, workspace=pws,
+                                        status=status, stream=stream, max_ctas=split[0])
+            cuda_lib.attn_decode_paged(q[256:], inp.k_pools[layer], inp.v_pools[layer],
+                                       inp.block_table[1:], inp.seq_lens[1:], max_s, inp.scale,
+                                       out=do, lse=dl, workspace=dws, status=status, stream=side,
+                                       max_ctas=split[1])
+            stream.wait_stream(side)
+
+    g = torch.cuda.CUDAGraph()
+    s0 = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s0):
+        with torch.cuda.graph(g):
+            step()
+    g.replay()  # the append is idempotent: the same tokens land in the same slots
+    torch.cuda.synchronize()
+    assert cuda_lib.read_device_status(status) == 0
+    for layer in range(2):
+        ro = oracle_mixed(inp, layer, kb[layer], vb[layer], 256)
+        po, pl, do, dl = outs[layer]
+        check_attn(po, pl, ro[0], ro[1], what=f"overlapped layer {layer} prefill {split}")
+        check_attn(do, dl, ro[2], ro[3], what=f"overlapped layer {layer} decode {split}")
