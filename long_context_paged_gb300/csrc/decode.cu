@@ -17,10 +17,12 @@
 //    V. A producer warp streams whole pages into a 3-stage shared-memory ring with bulk
 //    asynchronous copies (cp.async.bulk + mbarrier transaction counts): 64 KB per stage,
 //    up to 192 KB in flight per SM. Block-table entries are fetched 32 at a time.
-//  * Eight consumer warps, one per KV head; each serves BOTH query heads of its GQA group
-//    from one read of the K/V rows. Lane (c, th) holds dims 8c..8c+7 of tokens th*8..th*8+7.
-//    Scores are reduce-scattered across the 16 lanes of a half-warp (15 shuffles per page
-//    for 16 scores), so each lane ends with exactly one (token, head) score and one exp2.
+//  * Sixteen consumer warps, two per KV head, each taking 8 of a page's 16 tokens; each serves
+//    BOTH query heads of its GQA group from one read of the K/V rows. Lane (c, th) holds dims
+//    8c..8c+7 of 4 tokens. Scores are reduce-scattered across the 16 lanes of a half-warp
+//    (8 shuffles per page for 8 scores), so each lane ends with one (token, head) score. The
+//    two warps of a head keep their own running max and sums and merge once per (sequence,
+//    range) through shared memory.
 //  * fp32 math on bf16 loads, paired fp32 FMAs (fma.rn.f32x2). The running max is only moved
 //    when a page exceeds it by more than 8 (log2 units), so the accumulators are rescaled
 //    rarely; probabilities stay <= 2^8 and the result is exact up to rounding.
@@ -37,7 +39,11 @@
 namespace pa {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+// Two consumer warps per (KV head, page slot) pair, each taking half of every page's tokens: with
+// one warp per pair a CTA consumed a 64 KB stage in ~2,100 cycles (two warps per SMSP, bound by
+// their dependent latencies), which capped it at ~61 GB/s however few CTAs shared the HBM.
+constexpr int kPairs = 8;
+constexpr int kConsumerWarps = 2 * kPairs;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 3;
 // A ring stage holds K (or V) of 16 tokens x 8 KV heads: one page of the decoder's pools, or
@@ -51,13 +57,21 @@ constexpr int kMinPagesPerCta = 1;
 
 struct DecodeSmem {
   uint8_t kv[kStages][2][kStageBytes];
-  float p[kConsumerWarps][32];
+  alignas(16) float p[kConsumerWarps][16];
+  // hand-off of a (sequence, range)'s second token half to the first: per warp pair, lane l's
+  // 8 accumulator values and each head's max and sum
+  alignas(16) float xo[kPairs][32][8];
+  float xm[kPairs][2];
+  float xl[kPairs][2];
+  uint64_t xfull[kPairs];
+  uint64_t xempty[kPairs];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int32_t warp_tot[kThreads / 32];
   int32_t total;
   int32_t prefix[kMaxBatch + 1];
 };
+static_assert(sizeof(DecodeSmem) <= 227 * 1024, "decode shared memory beyond the per-CTA limit");
 
 struct DecodeParams {
   int32_t hq;           // query heads of the call (2 x its KV heads)
@@ -158,6 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kPairs; ++i) {
+      mbar_init(&s.xfull[i], 32);
+      mbar_init(&s.xempty[i], 32);
     }
     fence_mbar_init();
   }
@@ -265,13 +283,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
   }
 
   // ------------------------------------------------------------------ consumer warps
-  const int g = warp % kHkvT;  // KV head
-  const int slot = warp / kHkvT;  // page of each stage
-  const int c = lane & 15;     // dims 8c .. 8c+7
-  const int th = lane >> 4;    // tokens th*8 .. th*8+7 of each page
-  const bool hi_head = (c & 8) != 0;  // head of the score this lane owns after the scatter
+  // Warp w serves (KV head, page slot) pair w % 8 and tokens 8 * (w / 8) .. +7 of each page; the
+  // two warps of a pair keep their own running max, sums and accumulators and are merged once
+  // per (sequence, range) through shared memory.
+  const int pair = warp & 7;
+  const int half = warp >> 3;
+  const int g = pair % kHkvT;   // KV head
+  const int slot = pair / kHkvT;  // page of each stage
+  const int c = lane & 15;      // dims 8c .. 8c+7
+  const int th = lane >> 4;     // tokens tok0 .. tok0+3 of each page
+  const int tok0 = 8 * half + 4 * th;
+  // after the scatter lane c owns the score of token tok0 + (c & 3), head c >> 2 & 1 (lanes c and
+  // c ^ 8 hold the same one)
+  const bool hi_head = (c & 4) != 0;
   int stage = 0;
   uint32_t phase = 0;
+  uint32_t xphase = 0;  // hand-offs between the two warps of the pair so far, mod 2
 
   for (int rg = blockIdx.x; rg < n_ranges; rg += gridDim.x) {
     const int P0 = rg * W, P1 = min(total, P0 + W);
@@ -318,11 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
         const uint8_t* Ks = s.kv[stage][0] + slot * kPageBytes + g * (kHeadDim * 2) + c * 16;
         const uint8_t* Vs = s.kv[stage][1] + slot * kPageBytes + g * (kHeadDim * 2) + c * 16;
         if (active) {
-          // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
-          float v[16];
+          // ---- scores: partial dot products over this lane's 8 dims, for 4 tokens x 2 heads
+          float v[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 kr = lds128(Ks + (th * 8 + j) * kTokenBytes);
+          for (int j = 0; j < 4; ++j) {
+            const uint4 kr = lds128(Ks + (tok0 + j) * kTokenBytes);
             const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
             const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
             const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
@@ -332,12 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
             sa = fma2(qa[2], k2, sa); sb = fma2(qb[2], k2, sb);
             sa = fma2(qa[3], k3, sa); sb = fma2(qb[3], k3, sb);
             v[j] = sa.x + sa.y;
-            v[8 + j] = sb.x + sb.y;
+            v[4 + j] = sb.x + sb.y;
           }
-          // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score
-          //      of token th*8 + (c & 7), head (c >> 3).
+          // ---- reduce-scatter over lanes c & 7 of the half-warp, then add the other 8 dims'
+          //      lanes: lane c keeps the full score of value c & 7 (token tok0 + (c & 3), head
+          //      (c >> 2) & 1)
 #pragma unroll
-          for (int w = 8; w >= 1; w >>= 1) {
+          for (int w = 4; w >= 1; w >>= 1) {
             const bool up = (c & w) != 0;
 #pragma unroll
             for (int i = 0; i < w; ++i) {
@@ -346,15 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
               v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
             }
           }
-          float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
+          const float sc = (tok0 + (c & 3) < n_valid) ? v[0] : -CUDART_INF_F;
 
-          // ---- page max per head, lazily moved running max
+          // ---- page max per head over this warp's 8 tokens, lazily moved running max
           float pm = sc;
           pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
           pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
           pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-          const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
+          const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 4);
           const float pmax_a = hi_head ? pm_other : pm;
           const float pmax_b = hi_head ? pm : pm_other;
           if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
@@ -371,24 +399,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
             m_a = na;
             m_b = nb;
           }
-          const float pr = fast_exp2(sc - (hi_head ? m_b : m_a));
+          // (a warp may have seen only masked tokens so far when its half of a partial page is
+          // empty: its max is still -inf and the probability is 0)
+          const float mh = hi_head ? m_b : m_a;
+          const float pr = sc == -CUDART_INF_F ? 0.f : fast_exp2(sc - mh);
           l_part += pr;
 
-          // ---- hand probabilities to the lanes that own the V dims
-          s.p[warp][lane] = pr;
+          // ---- hand probabilities to the lanes that own the V dims: p[th * 8 + head * 4 + j]
+          if (c < 8) s.p[warp][th * 8 + c] = pr;
           __syncwarp();
-          const float4 pa0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 0]);
-          const float4 pa1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 4]);
-          const float4 pb0 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 8]);
-          const float4 pb1 = *reinterpret_cast<const float4*>(&s.p[warp][th * 16 + 12]);
-          const float pav[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
-          const float pbv[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
+          const float4 pa4 = *reinterpret_cast<const float4*>(&s.p[warp][th * 8]);
+          const float4 pb4 = *reinterpret_cast<const float4*>(&s.p[warp][th * 8 + 4]);
+          const float pav[4] = {pa4.x, pa4.y, pa4.z, pa4.w};
+          const float pbv[4] = {pb4.x, pb4.y, pb4.z, pb4.w};
 
-          // ---- o += p v over this lane's 8 tokens (invalid slots of a partial page skipped)
+          // ---- o += p v over this lane's 4 tokens (invalid slots of a partial page skipped)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (th * 8 + j < n_valid) {
-              const uint4 vr = lds128(Vs + (th * 8 + j) * kTokenBytes);
+          for (int j = 0; j < 4; ++j) {
+            if (tok0 + j < n_valid) {
+              const uint4 vr = lds128(Vs + (tok0 + j) * kTokenBytes);
               const float2 ppa = make_float2(pav[j], pav[j]);
               const float2 ppb = make_float2(pbv[j], pbv[j]);
               const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
@@ -408,15 +437,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
       }
       if (!all_ok) return;
 
-      // ---- finish this (sequence, range): denominators and the two token halves
+      // ---- finish this warp's half: sums over its 8 tokens (lanes c and c ^ 8 hold the same
+      //      probabilities, so they are not added together) and over the two token quarters
       float l_m = l_part;
       l_m += __shfl_xor_sync(0xffffffffu, l_m, 1);
       l_m += __shfl_xor_sync(0xffffffffu, l_m, 2);
-      l_m += __shfl_xor_sync(0xffffffffu, l_m, 4);
       l_m += __shfl_xor_sync(0xffffffffu, l_m, 16);
-      const float l_o = __shfl_xor_sync(0xffffffffu, l_m, 8);
-      const float l_a = hi_head ? l_o : l_m;
-      const float l_b = hi_head ? l_m : l_o;
+      const float l_o = __shfl_xor_sync(0xffffffffu, l_m, 4);
+      float l_a = hi_head ? l_o : l_m;
+      float l_b = hi_head ? l_m : l_o;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc_a[i].x += __shfl_xor_sync(0xffffffffu, acc_a[i].x, 16);
@@ -426,18 +455,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
       }
       // lanes 0..15 finish head 2g, lanes 16..31 head 2g+1
       const int head = 2 * g + th;
-      const float l_h = th ? l_b : l_a;
-      const float m_h = th ? m_b : m_a;
-      // (with several pages per stage a warp may have seen no page of this range: l = 0, and
-      // its record is o = 0, lse = -inf, which the merge weighs by 0)
-      const float inv = (kSlots == 1 || l_h > 0.f) ? 1.0f / l_h : 0.f;
+      float m_h = th ? m_b : m_a;
+      float l_h = th ? l_b : l_a;
       float o[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 a = th ? acc_b[i] : acc_a[i];
-        o[2 * i] = a.x * inv;
-        o[2 * i + 1] = a.y * inv;
+        o[2 * i] = a.x;
+        o[2 * i + 1] = a.y;
       }
+
+      // ---- the second half hands its (max, sum, accumulator) to the first, which merges them
+      bool xok = true;
+      if (half == 1) {
+        if (!mbar_wait_bounded(&s.xempty[pair], xphase ^ 1u, p.wait_limit_ns)) xok = false;
+        if (xok) {
+          float4* dst = reinterpret_cast<float4*>(s.xo[pair][lane]);
+          dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+          if (c == 0) {
+            s.xm[pair][th] = m_h;
+            s.xl[pair][th] = l_h;
+          }
+          mbar_arrive(&s.xfull[pair]);
+        }
+      } else {
+        if (!mbar_wait_bounded(&s.xfull[pair], xphase, p.wait_limit_ns)) xok = false;
+        if (xok) {
+          const float4* src = reinterpret_cast<const float4*>(s.xo[pair][lane]);
+          const float4 u0 = src[0], u1 = src[1];
+          const float m1 = s.xm[pair][th], l1 = s.xl[pair][th];
+          mbar_arrive(&s.xempty[pair]);
+          const float mm = fmaxf(m_h, m1);
+          const float al0 = (m_h == -CUDART_INF_F) ? 0.f : fast_exp2(m_h - mm);
+          const float al1 = (m1 == -CUDART_INF_F) ? 0.f : fast_exp2(m1 - mm);
+          const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = o[i] * al0 + u[i] * al1;
+          l_h = l_h * al0 + l1 * al1;
+          m_h = mm;
+        }
+      }
+      xphase ^= 1u;
+      if (!__all_sync(0xffffffffu, xok)) {
+        flag_error(p.status, PA_DEV_ERR_TIMEOUT);
+        return;
+      }
+      if (half == 1) continue;
+
+      // (with several pages per stage a warp pair may have seen no page of this range: l = 0,
+      // and its record is o = 0, lse = -inf, which the merge weighs by 0)
+      const float inv = (kSlots == 1 || l_h > 0.f) ? 1.0f / l_h : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] *= inv;
       const float lse_h = (m_h + log2f(l_h)) * kLn2;
       if (kSlots == 1 && lp0 == 0 && lp1 == n_pages) {
         uint4 w;
