@@ -86,6 +86,7 @@ constexpr int kLaunchRegs = (256 * kSoftmaxRegs + 128 * kControlRegs) / kThreads
 // are adjacent, so a warp's 32 rows store and load 512 contiguous bytes), then lse [2][128] fp32.
 constexpr size_t kRecordO = 2 * 128 * 128 * sizeof(float);
 constexpr size_t kRecordBytes = kRecordO + 2 * 128 * sizeof(float);
+constexpr int kMergeRows = 128;  // threads of a merge CTA: one per row of a query tile
 
 // One piece of the walk as the roles use it: key tiles [jb, je) of job (b, g, qt), with the
 // chunk's first packed row q0, its length n, the sequence's keys L and the chunk's offset off;
@@ -957,32 +958,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
   }
 }
 
-// Combine the pieces of jobs that were cut by CTA range boundaries. One CTA per job; thread =
-// (head, row). The pieces are slot 1 of the first CTA and slot 0 of each later CTA.
-__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParams p) {
+// Combine the pieces of jobs that were cut by CTA range boundaries. Eight CTAs per job (two
+// heads x four 32-dim quarters), one thread per row. The pieces are slot 1 of the first CTA and
+// slot 0 of each later CTA.
+__global__ void __launch_bounds__(kMergeRows) prefill_merge_kernel(const PrefillTcParams p) {
   // programmatic dependent of prefill_tc_kernel: wait until that grid is complete and visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.z, g = blockIdx.y, qt = blockIdx.x;
+  // CTA (qt, g * 8 + t * 4 + quarter, b), counted from the end of the grid: rows of query tile
+  // qt, head 2g + t, dims 32 * quarter .. +31; one thread per row. A job cut into pieces is
+  // merged by 8 CTAs, so the few split jobs of a call are spread over many SMs instead of one CTA
+  // each. The split jobs are the last ones (the whole-job rounds take the first), so the grid is
+  // walked backwards: their CTAs start first and the rest only check and exit.
+  const int b = gridDim.z - 1 - blockIdx.z;
+  const int y = gridDim.y - 1 - blockIdx.y;
+  const int g = y >> 3, t = (y >> 2) & 1, quarter = y & 3;
+  const int qt = gridDim.x - 1 - blockIdx.x;
   const SeqGeom s = seq_geom(p, b, false);
   if (qt >= s.nqt) return;
   const int jo = p.ws_job_prefix[b] + g * s.nqt + qt;
   if (jo < p.ws_header[3]) return;  // done whole in the round-robin phase
-  const int G = static_cast<int>(p.ws_header[0]);
+  const int G = min(static_cast<int>(p.ws_header[0]), kThreads);  // the prefill grid, <= kThreads
   const long long u0 = p.ws_prefix[b] + g * s.T + units_before(s, qt);
   const long long J = tiles_of(s, qt);
-  // the CTA whose range [ws_tail[c], ws_tail[c + 1]) holds unit u (the last c with a start <= u:
-  // a CTA with an empty range shares its start with the next one)
+  // the split's range starts, staged in shared memory: one round of loads instead of a chain of
+  // dependent ones per binary search
+  __shared__ long long tail[kThreads + 1];
+  for (int i = threadIdx.x; i <= G; i += kMergeRows) tail[i] = p.ws_tail[i];
+  __syncthreads();
+  // the CTA whose range [tail[c], tail[c + 1]) holds unit u (the last c with a start <= u: a CTA
+  // with an empty range shares its start with the next one)
   auto cta_of = [&](long long u) {
     int lo = 0, hi = G;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (p.ws_tail[mid] <= u) lo = mid; else hi = mid;
+      if (tail[mid] <= u) lo = mid; else hi = mid;
     }
     return lo;
   };
   const int c0 = cta_of(u0), c1 = cta_of(u0 + J - 1);
   if (c0 == c1) return;
-  const int t = threadIdx.x >> 7, r = threadIdx.x & 127;
+  const int r = threadIdx.x;
   const int qrow = qt * kTileM + r;
   if (qrow >= s.n) return;
   // the piece in CTA c0 starts the job (slot 1); later CTAs hold continuations (slot 0); CTAs with
@@ -990,14 +1005,15 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
   auto rec_of = [&](int c) {
     return p.ws_records + (2 * static_cast<size_t>(c) + (c == c0 ? 1 : 0)) * kRecordBytes;
   };
-  auto empty_range = [&](int c) { return p.ws_tail[c] == p.ws_tail[c + 1]; };
+  auto empty_range = [&](int c) { return tail[c] == tail[c + 1]; };
   float m = -CUDART_INF_F;
   for (int c = c0; c <= c1; ++c)
     if (!empty_range(c)) m = fmaxf(m, reinterpret_cast<const float*>(rec_of(c) + kRecordO)[t * 128 + r]);
-  float acc[kHeadDim];
+  float acc[32];
 #pragma unroll
-  for (int d = 0; d < kHeadDim; ++d) acc[d] = 0.f;
+  for (int d = 0; d < 32; ++d) acc[d] = 0.f;
   float sum = 0.f;
+#pragma unroll 2
   for (int c = c0; c <= c1; ++c) {
     if (empty_range(c)) continue;
     const uint8_t* rec = rec_of(c);
@@ -1005,21 +1021,24 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
     if (lp == -CUDART_INF_F) continue;  // the piece held no key visible to this row
     const float w = fast_exp2((lp - m) * kLog2e);
     sum += w;
-    const float4* o = reinterpret_cast<const float4*>(rec) + t * 32 * 128 + r;
+    const float4* o = reinterpret_cast<const float4*>(rec) + (t * 32 + quarter * 8) * 128 + r;
+    float4 v[8];
 #pragma unroll
-    for (int d = 0; d < kHeadDim / 4; ++d) {
-      const float4 v = o[d * 128];
-      acc[4 * d] += w * v.x;
-      acc[4 * d + 1] += w * v.y;
-      acc[4 * d + 2] += w * v.z;
-      acc[4 * d + 3] += w * v.w;
+    for (int d = 0; d < 8; ++d) v[d] = o[d * 128];
+#pragma unroll
+    for (int d = 0; d < 8; ++d) {
+      acc[4 * d] += w * v[d].x;
+      acc[4 * d + 1] += w * v[d].y;
+      acc[4 * d + 2] += w * v[d].z;
+      acc[4 * d + 3] += w * v[d].w;
     }
   }
   const float inv = 1.0f / sum;
   const int head = 2 * g + t;
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(s.q0 + qrow) * p.hq + head) * kHeadDim);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(s.q0 + qrow) * p.hq + head) * kHeadDim +
+                                        32 * quarter);
 #pragma unroll
-  for (int k = 0; k < kHeadDim / 8; ++k) {
+  for (int k = 0; k < 4; ++k) {
     uint4 w;
     w.x = pack_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
     w.y = pack_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
@@ -1027,7 +1046,8 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillTcParam
     w.w = pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
     dst[k] = w;
   }
-  if (p.lse != nullptr) p.lse[static_cast<int64_t>(s.q0 + qrow) * p.hq + head] = m + logf(sum);
+  if (quarter == 0 && p.lse != nullptr)
+    p.lse[static_cast<int64_t>(s.q0 + qrow) * p.hq + head] = m + logf(sum);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1134,8 +1154,8 @@ pa_status launch_prefill_tc(int32_t hkv, const void* q, int32_t total_q, const i
   prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(qm, km, vm, p);
   PA_CHECK_LAUNCH("prefill_tc_kernel");
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((max_q_len + kTileM - 1) / kTileM, hkv, batch);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((max_q_len + kTileM - 1) / kTileM, hkv * 8, batch);
+  cfg.blockDim = dim3(kMergeRows);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
