@@ -32,6 +32,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "cluster_common.cuh"
 #include "pa_common.cuh"
@@ -57,7 +58,7 @@ constexpr int kMinPagesPerCta = 1;
 
 struct DecodeSmem {
   uint8_t kv[kStages][2][kStageBytes];
-  alignas(16) float p[kConsumerWarps][16];
+  alignas(16) float2 p2[kConsumerWarps][16];  // probabilities, each as a (p, p) pair
   // hand-off of a (sequence, range)'s second token half to the first: per warp pair, lane l's
   // 8 accumulator values and each head's max and sum
   alignas(16) float xo[kPairs][32][8];
@@ -344,7 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
         }
         const uint8_t* Ks = s.kv[stage][0] + slot * kPageBytes + g * (kHeadDim * 2) + c * 16;
         const uint8_t* Vs = s.kv[stage][1] + slot * kPageBytes + g * (kHeadDim * 2) + c * 16;
-        if (active) {
+        // One page of this warp's tokens; kFull: all of them are keys (every page but a sequence's
+        // last), so no token is masked or skipped.
+        auto page = [&](auto full_tag) {
+          constexpr bool kFull = decltype(full_tag)::value;
           // ---- scores: partial dot products over this lane's 8 dims, for 4 tokens x 2 heads
           float v[8];
 #pragma unroll
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
             }
           }
           v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
-          const float sc = (tok0 + (c & 3) < n_valid) ? v[0] : -CUDART_INF_F;
+          const float sc = (kFull || tok0 + (c & 3) < n_valid) ? v[0] : -CUDART_INF_F;
 
           // ---- page max per head over this warp's 8 tokens, lazily moved running max
           float pm = sc;
@@ -400,36 +404,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
             m_b = nb;
           }
           // (a warp may have seen only masked tokens so far when its half of a partial page is
-          // empty: its max is still -inf and the probability is 0)
+          // empty: its max is still -inf and the probability is 0; on a full page the max is
+          // finite by now)
           const float mh = hi_head ? m_b : m_a;
-          const float pr = sc == -CUDART_INF_F ? 0.f : fast_exp2(sc - mh);
+          const float pr = (!kFull && sc == -CUDART_INF_F) ? 0.f : fast_exp2(sc - mh);
           l_part += pr;
 
-          // ---- hand probabilities to the lanes that own the V dims: p[th * 8 + head * 4 + j]
-          if (c < 8) s.p[warp][th * 8 + c] = pr;
+          // ---- hand probabilities to the lanes that own the V dims, each stored twice (the
+          //      paired FMAs take it as both halves): p2[th * 8 + head * 4 + j]
+          if (c < 8) s.p2[warp][th * 8 + c] = make_float2(pr, pr);
           __syncwarp();
-          const float4 pa4 = *reinterpret_cast<const float4*>(&s.p[warp][th * 8]);
-          const float4 pb4 = *reinterpret_cast<const float4*>(&s.p[warp][th * 8 + 4]);
-          const float pav[4] = {pa4.x, pa4.y, pa4.z, pa4.w};
-          const float pbv[4] = {pb4.x, pb4.y, pb4.z, pb4.w};
+          float2 ppa[4], ppb[4];
+#pragma unroll
+          for (int j = 0; j < 4; j += 2) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&s.p2[warp][th * 8 + j]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&s.p2[warp][th * 8 + 4 + j]);
+            ppa[j] = make_float2(a4.x, a4.y);
+            ppa[j + 1] = make_float2(a4.z, a4.w);
+            ppb[j] = make_float2(b4.x, b4.y);
+            ppb[j + 1] = make_float2(b4.z, b4.w);
+          }
 
           // ---- o += p v over this lane's 4 tokens (invalid slots of a partial page skipped)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            if (tok0 + j < n_valid) {
+            if (kFull || tok0 + j < n_valid) {
               const uint4 vr = lds128(Vs + (tok0 + j) * kTokenBytes);
-              const float2 ppa = make_float2(pav[j], pav[j]);
-              const float2 ppb = make_float2(pbv[j], pbv[j]);
               const float2 v0 = make_float2(bf16lo(vr.x), bf16hi(vr.x));
               const float2 v1 = make_float2(bf16lo(vr.y), bf16hi(vr.y));
               const float2 v2 = make_float2(bf16lo(vr.z), bf16hi(vr.z));
               const float2 v3 = make_float2(bf16lo(vr.w), bf16hi(vr.w));
-              acc_a[0] = fma2(v0, ppa, acc_a[0]); acc_b[0] = fma2(v0, ppb, acc_b[0]);
-              acc_a[1] = fma2(v1, ppa, acc_a[1]); acc_b[1] = fma2(v1, ppb, acc_b[1]);
-              acc_a[2] = fma2(v2, ppa, acc_a[2]); acc_b[2] = fma2(v2, ppb, acc_b[2]);
-              acc_a[3] = fma2(v3, ppa, acc_a[3]); acc_b[3] = fma2(v3, ppb, acc_b[3]);
+              acc_a[0] = fma2(v0, ppa[j], acc_a[0]); acc_b[0] = fma2(v0, ppb[j], acc_b[0]);
+              acc_a[1] = fma2(v1, ppa[j], acc_a[1]); acc_b[1] = fma2(v1, ppb[j], acc_b[1]);
+              acc_a[2] = fma2(v2, ppa[j], acc_a[2]); acc_b[2] = fma2(v2, ppb[j], acc_b[2]);
+              acc_a[3] = fma2(v3, ppa[j], acc_a[3]); acc_b[3] = fma2(v3, ppb[j], acc_b[3]);
             }
           }
+        };
+        if (n_valid == kPage) {
+          page(std::true_type{});
+        } else if (active) {
+          page(std::false_type{});
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.empty[stage]);
