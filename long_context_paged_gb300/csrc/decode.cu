@@ -158,7 +158,8 @@ __device__ __forceinline__ int find_seq(const int32_t* prefix, int batch, int x)
 }
 
 // kHkvT: KV heads of the call (8 for the decoder; 1, 2 or 4 for a device's share of them).
-// Consumer warp w serves KV head w % kHkvT of page slot w / kHkvT of each stage.
+// Consumer warp w serves KV head (w % 8) % kHkvT of page slot (w % 8) / kHkvT of each stage, tokens
+// 8 * (w / 8) .. +7 of each page.
 template <int kHkvT>
 __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const DecodeParams p) {
   constexpr int kSlots = kHkv / kHkvT;                        // pages per stage
