@@ -804,32 +804,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         }
         tc::fence_after_sync();
         uint32_t sb[128];  // raw scores (fp32 bits) of this row
+        float cm[4];       // the maximum of each 32-column piece, from the TMEM load itself
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sb + c * 32));
+          tc::tmem_ld32_max(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sb + c * 32), cm[c]);
         tc::tmem_wait_ld();
         const int k0 = (pjb + i) * kTileN;
+        float mx = fmax3(cm[0], cm[1], fmaxf(cm[2], cm[3]));
         if (k0 + kTileN - 1 > qpos) {
+          // the tile crosses this row's position: mask the keys after the query, then take the
+          // row max over what is left (8 independent partial maxima, two new elements per
+          // three-input max)
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (k0 + c > qpos) sb[c] = 0xff800000u;  // -inf: key after this query
-        }
-        // row max over 8 independent partial maxima (no 128-long dependency chain), two new
-        // elements per three-input max
-        float pm[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          pm[k] = fmax3(__uint_as_float(sb[k]), __uint_as_float(sb[k + 8]), __uint_as_float(sb[k + 16]));
-#pragma unroll
-        for (int c = 24; c < 120; c += 16) {
+          float pm[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            pm[k] = fmax3(pm[k], __uint_as_float(sb[c + k]), __uint_as_float(sb[c + 8 + k]));
-        }
+            pm[k] = fmax3(__uint_as_float(sb[k]), __uint_as_float(sb[k + 8]), __uint_as_float(sb[k + 16]));
 #pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], __uint_as_float(sb[120 + k]));
-        const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                               fmaxf(pm[6], pm[7]));
+          for (int c = 24; c < 120; c += 16) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              pm[k] = fmax3(pm[k], __uint_as_float(sb[c + k]), __uint_as_float(sb[c + 8 + k]));
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], __uint_as_float(sb[120 + k]));
+          mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+        }
         const float mx2 = mx * p.scale_log2;
         const bool grow = mx2 > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, grow)) {
