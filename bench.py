@@ -475,7 +475,7 @@ def main():
     ap.add_argument("--clocks-out", default=None)
     ap.add_argument("--decode-ctas", type=int, default=-1,
                     help="whole-step graph: CTAs of each layer's decode, run on a second stream "
-                         "beside the prefill on the other SMs (-1: 45%% of the SMs; 0: one after "
+                         "beside the prefill on the other SMs (-1: 43.5%% of the SMs; 0: one after "
                          "the other)")
     args = ap.parse_args()
 
@@ -515,7 +515,7 @@ def main():
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     step_split = None
     if has_dec and has_pf and args.decode_ctas != 0:
-        nd = round(0.45 * sms) if args.decode_ctas < 0 else min(args.decode_ctas, sms - 1)
+        nd = round(0.435 * sms) if args.decode_ctas < 0 else min(args.decode_ctas, sms - 1)
         step_split = (sms - nd, nd)
     g_step = capture(step, ("append", "prefill", "decode"), split=step_split)
     g_dec = capture(step, ("decode",)) if has_dec else None
