@@ -122,3 +122,42 @@ def test_prefill_chunk_longer_than_sequence_is_flagged(cuda_lib):
     cuda_lib.attn_prefill_chunk(inp.q[0], inp.cu_q_lens, inp.k_pools[0], inp.v_pools[0],
                                 inp.block_table, sl, 20, 50, inp.scale, status=status)
     assert cuda_lib.read_device_status(status) & cuda_lib.DEV_ERR_LENGTH
+
+
+def test_prefill_dominant_key_in_each_column_piece(cuda_lib):
+    """Every query of a head pair sees the same scores and one key that dominates them: each row
+    that sees the key returns its V row bit for bit. The dominant keys sit in each 32-column
+    piece of a 128-key tile (the row max of a piece comes from the TMEM load on tiles that do not
+    cross the row's position), on tiles both before the chunk and on its diagonal; the rows that
+    do not see their key yet, and the head pair without one, are checked against the oracle."""
+    offset, q_len = 1024, 256
+    inp = W.make_paged(303, [offset + q_len], [q_len], poison=True, device="cuda")
+    q = inp.q[0]
+    k = inp.k_pools[0]
+    bt = inp.host_block_table
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    # KV head g -> position of its dominant key (None: no dominant key)
+    dominant = {0: 5, 1: 128 + 32 + 5, 2: 256 + 64 + 5, 3: 384 + 96 + 5,
+                4: offset + 10, 5: offset + 128 + 70, 6: offset + 127, 7: None}
+    for g, t in dominant.items():
+        if t is None:
+            continue
+        q0 = torch.randn(W.HEAD_DIM, generator=gen, device="cuda").to(torch.bfloat16)
+        q[:, 2 * g] = q0
+        q[:, 2 * g + 1] = q0
+        page, slot = int(bt[0, t // W.PAGE]), t % W.PAGE
+        k[page, slot, g] = (64.0 * torch.sign(q0.float())).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefill(cuda_lib, inp, status=status)
+    assert cuda_lib.read_device_status(status) == 0
+    v = inp.v_pools[0]
+    for g, t in dominant.items():
+        if t is None:
+            continue
+        page, slot = int(bt[0, t // W.PAGE]), t % W.PAGE
+        first_row = max(0, t - offset)   # the first query whose position reaches the key
+        for h in (2 * g, 2 * g + 1):
+            want = v[page, slot, g].expand(q_len - first_row, W.HEAD_DIM)
+            assert torch.equal(out[first_row:, h], want), (g, t, h)
+    ref_o, ref_l = oracle_prefill(inp)
+    check_attn(out, lse, ref_o, ref_l, what="dominant keys")
