@@ -100,6 +100,14 @@ struct DecodeParams {
   int32_t starve;          // test hook: CTA 0 never fills its first ring stage
 };
 
+// Maximum of v over the 32 lanes of the warp, in every lane (redux.sync on fp32, sm_100 and
+// later; like fmaxf, a NaN operand is ignored when another lane holds a number).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // Keys of sequence b as the kernels use them: negative -> 0, more than the table row covers
 // -> cut to bt_stride * 16 (both flagged).
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, bool report) {
@@ -382,14 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
           v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
           const float sc = (kFull || tok0 + (c & 3) < n_valid) ? v[0] : -CUDART_INF_F;
 
-          // ---- page max per head over this warp's 8 tokens, lazily moved running max
-          float pm = sc;
-          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
-          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-          const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 4);
-          const float pmax_a = hi_head ? pm_other : pm;
-          const float pmax_b = hi_head ? pm : pm_other;
+          // ---- page max per head over this warp's 8 tokens (one warp-wide max reduction per
+          //      head), lazily moved running max
+          const float pmax_a = warp_max(hi_head ? -CUDART_INF_F : sc);
+          const float pmax_b = warp_max(hi_head ? sc : -CUDART_INF_F);
           if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
             const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
             const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
