@@ -916,15 +916,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
       }
     }
     const float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
-    // ---- page max per head, lazily moved running max (at least one key of a page is valid)
-    float pm = sc;
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-    const float pm_other = __shfl_xor_sync(0xffffffffu, pm, 8);
-    const float pmax_a = hi_head ? pm_other : pm;
-    const float pmax_b = hi_head ? pm : pm_other;
+    // ---- page max per head (one warp-wide max reduction per head), lazily moved running max
+    //      (at least one key of a page is valid)
+    const float pmax_a = warp_max(hi_head ? -CUDART_INF_F : sc);
+    const float pmax_b = warp_max(hi_head ? sc : -CUDART_INF_F);
     if (pmax_a > m_a + kRescaleThreshold || pmax_b > m_b + kRescaleThreshold) {
       const float na = fmaxf(m_a, pmax_a), nb = fmaxf(m_b, pmax_b);
       const float al_a = (m_a == -CUDART_INF_F) ? 0.f : fast_exp2(m_a - na);
