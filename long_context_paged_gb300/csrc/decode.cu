@@ -320,11 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
       if (lp0 >= lp1) continue;
       const int L = clamp_len(p, b, false);
 
+      // q of the two heads in this lane's order: its own head (the one whose score it keeps
+      // after the scatter) first
       float2 qa[4], qb[4];
       {
         const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHqT + 2 * g) * kHeadDim + 8 * c;
-        const uint4 ra = *reinterpret_cast<const uint4*>(qrow);
-        const uint4 rb = *reinterpret_cast<const uint4*>(qrow + kHeadDim);
+        const uint4 ra = *reinterpret_cast<const uint4*>(qrow + (hi_head ? kHeadDim : 0));
+        const uint4 rb = *reinterpret_cast<const uint4*>(qrow + (hi_head ? 0 : kHeadDim));
         const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -358,11 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
         // last), so no token is masked or skipped.
         auto page = [&](auto full_tag) {
           constexpr bool kFull = decltype(full_tag)::value;
-          // ---- scores: partial dot products over this lane's 8 dims, for 4 tokens x 2 heads
+          // ---- scores: partial dot products over this lane's 8 dims, for 4 tokens x 2 heads.
+          //      Register i holds value k = i ^ (c & 7) (k = head * 4 + token, head 0 = 2g): the
+          //      lane visits its tokens as j ^ (c & 3) and its own head first, so that every lane
+          //      keeps the low half of its values and sends the high half in each scatter round.
           float v[8];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint4 kr = lds128(Ks + (tok0 + j) * kTokenBytes);
+            const uint4 kr = lds128(Ks + (tok0 + (j ^ (c & 3))) * kTokenBytes);
             const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
             const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
             const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
@@ -374,18 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
             v[j] = sa.x + sa.y;
             v[4 + j] = sb.x + sb.y;
           }
-          // ---- reduce-scatter over lanes c & 7 of the half-warp, then add the other 8 dims'
+          // ---- reduce-scatter over lanes c & 7 of the half-warp (register i of lane c and
+          //      register w + i of lane c ^ w hold the same value), then add the other 8 dims'
           //      lanes: lane c keeps the full score of value c & 7 (token tok0 + (c & 3), head
           //      (c >> 2) & 1)
 #pragma unroll
           for (int w = 4; w >= 1; w >>= 1) {
-            const bool up = (c & w) != 0;
 #pragma unroll
-            for (int i = 0; i < w; ++i) {
-              const float send = up ? v[i] : v[w + i];
-              const float keep = up ? v[w + i] : v[i];
-              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-            }
+            for (int i = 0; i < w; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[w + i], w);
           }
           v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
           const float sc = (kFull || tok0 + (c & 3) < n_valid) ? v[0] : -CUDART_INF_F;
@@ -824,11 +825,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
   // ---- this lane's share of the group's two query rows (dims 8c .. 8c+7), in log2 units
   const int c = lane & 15, th = lane >> 4;
   const bool hi_head = (c & 8) != 0;
+  // q of the two heads in this lane's order: its own head (the one whose score it keeps after the
+  // scatter) first
   float2 qa[4], qb[4];
   {
     const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * kHqT + 2 * g) * kHeadDim + 8 * c;
-    const uint4 ra = *reinterpret_cast<const uint4*>(qrow);
-    const uint4 rb = *reinterpret_cast<const uint4*>(qrow + kHeadDim);
+    const uint4 ra = *reinterpret_cast<const uint4*>(qrow + (hi_head ? kHeadDim : 0));
+    const uint4 rb = *reinterpret_cast<const uint4*>(qrow + (hi_head ? 0 : kHeadDim));
     const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -887,11 +890,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
     else if (ahead == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
     else asm volatile("cp.async.wait_group 0;" ::: "memory");
     const int n_valid = min(kPage, L - lp * kPage);
-    // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads
+    // ---- scores: partial dot products over this lane's 8 dims, for 8 tokens x 2 heads.
+    //      Register i holds value k = i ^ (c & 15) (k = head * 8 + token, head 0 = 2g): the lane
+    //      visits its tokens as j ^ (c & 7) and its own head first, so that every lane keeps the
+    //      low half of its values and sends the high half in each scatter round.
     float v[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint4 kr = lds128(slot(st, 0, j));
+      const uint4 kr = lds128(slot(st, 0, j ^ (c & 7)));
       const float2 k0 = make_float2(bf16lo(kr.x), bf16hi(kr.x));
       const float2 k1 = make_float2(bf16lo(kr.y), bf16hi(kr.y));
       const float2 k2 = make_float2(bf16lo(kr.z), bf16hi(kr.z));
@@ -903,17 +909,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_cluster_kernel(const 
       v[j] = sa.x + sa.y;
       v[8 + j] = sb.x + sb.y;
     }
-    // ---- reduce-scatter over the 16 lanes of the half-warp: lane c keeps the full score of
-    //      token th*8 + (c & 7), head (c >> 3)
+    // ---- reduce-scatter over the 16 lanes of the half-warp (register i of lane c and register
+    //      w + i of lane c ^ w hold the same value): lane c keeps the full score of token
+    //      th*8 + (c & 7), head (c >> 3)
 #pragma unroll
     for (int w = 8; w >= 1; w >>= 1) {
-      const bool up = (c & w) != 0;
 #pragma unroll
-      for (int i = 0; i < w; ++i) {
-        const float send = up ? v[i] : v[w + i];
-        const float keep = up ? v[w + i] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-      }
+      for (int i = 0; i < w; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[w + i], w);
     }
     const float sc = (th * 8 + (c & 7) < n_valid) ? v[0] : -CUDART_INF_F;
     // ---- page max per head (one warp-wide max reduction per head), lazily moved running max
