@@ -197,14 +197,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
   // completion), so it may be launched as soon as every CTA of this grid has got here (the
   // lengths it reads before that wait are final by now)
   asm volatile("griddepcontrol.launch_dependents;");
-  build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
-
-  const int total = s.total;
   // pages per range: an equal share per CTA (at least kMinPagesPerCta) unless a split size was
   // given; never fewer than the workspace has records for. A short batch is spread over as many
   // SMs as it has pages: one SM ingests a 32 KB page in well under a microsecond, so a
   // single-sequence decode is latency-bound, and its partials merge in parallel per head.
   const int base = p.split_pages > 0 ? p.split_pages : kMinPagesPerCta;
+  // One sequence (a single long request): if its length fills the host's bound to the page,
+  // the producer's first block-table entries follow from the bound alone, so they are loaded
+  // beside the length instead of after it, and used only once the length confirms them.
+  const int total_spec = (p.max_seq_len + kPage - 1) / kPage;
+  int spec_entry = 0;
+  if (p.batch == 1 && warp == kConsumerWarps) {
+    const int W_s = max((total_spec + p.max_ranges - 1) / p.max_ranges, base);
+    const int P0_s = static_cast<int>(blockIdx.x) * W_s;
+    if (lane < min(W_s, total_spec - P0_s) && P0_s + lane < p.bt_stride)
+      spec_entry = p.block_table[P0_s + lane];
+  }
+  build_prefix(p, s);  // ends with __syncthreads(), which also publishes the barrier init
+
+  const int total = s.total;
   const int W = max((total + p.max_ranges - 1) / p.max_ranges, base);
   if (blockIdx.x == 0) {
     if (tid == 0) {
@@ -234,9 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Decod
         const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
         for (int lp = lp0; ok && lp < lp1; lp += 32) {
           const int n = min(32, lp1 - lp);
+          // the entries loaded before the length are this CTA's first 32 when the length gave
+          // the same page count as the bound (then W and this range are the ones assumed)
+          const bool spec = p.batch == 1 && total == total_spec && rg == static_cast<int>(blockIdx.x) &&
+                            lp == lp0;
           int entry = 0;
           if (lane < n) {
-            entry = bt_row[lp + lane];
+            entry = spec ? spec_entry : bt_row[lp + lane];
             if (entry < 0 || entry >= p.num_pages) {
               flag_error(p.status, PA_DEV_ERR_PAGE_OOB);
               entry = 0;
