@@ -281,3 +281,23 @@ def test_binding_rejects_misshaped_buffers(cuda_lib):
         pa.attn_prefill_chunk(q, inp.cu_q_lens, kp, vp, inp.block_table, inp.seq_lens, 1, 200,
                               inp.scale, out=torch.empty(1, 16, 128, dtype=torch.bfloat16,
                                                          device="cuda"))
+
+
+@pytest.mark.parametrize("L,extra,split", [(30000, 0, 0), (30001, 7, 0), (30000, 100, 0),
+                                           (70000, 0, 0), (5000, 0, 256), (12345, 3, 4096)])
+def test_decode_one_sequence_against_its_length_bound(cuda_lib, L, extra, split):
+    """One sequence through the split-KV kernel with the host's length bound equal to its length,
+    above it within the same last page, and pages above it (past the end of the block-table
+    row): the block-table entries a CTA loads beside the length are used only when the length
+    gives the bound's page count, and every result matches the oracle."""
+    pa = cuda_lib
+    inp = W.make_paged(400 + L % 97, [L], [1], poison=True, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = pa.attn_decode_paged(inp.q[0], inp.k_pools[0], inp.v_pools[0], inp.block_table,
+                                    inp.seq_lens, L + extra, inp.scale, split_tokens=split,
+                                    status=status)
+    torch.cuda.synchronize()
+    assert pa.decode_kernels_per_call(1, L + extra, split) == 2
+    ref_o, ref_l = oracle_decode(inp)
+    check_attn(out, lse, ref_o, ref_l, what=f"one sequence of {L} keys, bound {L + extra}")
+    assert pa.read_device_status(status) == 0
